@@ -1,0 +1,392 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged FP8 latent-KV MLA decode step on GB300.
+
+One step = one mla_decode_paged call (split-KV decode kernel + split combine)
+over the whole batch of the TP8-shape workload: 8 requests x 12 heads x 1
+query position, 32,768 cached positions each, page 64, block table randomly
+permuted, FP8 E4M3FN latents (576 B per position), bf16 queries.
+
+Metric: latent-KV GB/s = (KV bytes the step must read) / (step time), plus
+decode steps/s and the fraction of the HBM roofline.  Inputs are resident in
+HBM; L2 is defeated by rotating several cache copies whose total exceeds L2.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the FP64 CPU oracle on host cores
+
+Multi-GPU (torchrun, one rank per GPU): every rank decodes its own batch of
+the same shape (independent requests, no collective on the data path);
+value = bytes of all ranks / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+HBM_NOMINAL_GBS = 8000.0  # the post's and the spec sheet's 8 TB/s
+METRIC = "latent-KV GB/s (KV bytes read / decode-step time); decode steps/s; % of 8 TB/s HBM"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="tp8_batch")
+    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tcgen05"])
+    ap.add_argument("--n-splits", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def workload_description(name):
+    from mla_latent_kv_fp8_gb300 import synth
+    return synth.WORKLOADS[name][0]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, copy burst)"
+    return 6800.0, "fallback (6.8 TB/s)"
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mla_latent_kv_fp8_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_family, workload):
+    """DRAM bytes per launch from a committed ncu summary, if its kernel source matches."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(f"{kernel_family}/{workload}")
+    if not e or e.get("source_sha") != kernel_source_sha():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"mla_bench_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = sorted(float(r[1]) for r in rows if r[1].replace(".", "").isdigit())
+        mx = max((float(r[2]) for r in rows if r[2].replace(".", "").isdigit()), default=None)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": mx, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+def make_inputs(name, device):
+    from mla_latent_kv_fp8_gb300 import synth
+    return synth.workload_case(name, device=device)
+
+
+def run_ours(args):
+    import torch
+    from mla_latent_kv_fp8_gb300 import _lib, synth
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    L = _lib
+    L.lib()
+    impl = {"auto": 0, "simt": 1, "tcgen05": 2}[args.kernel]
+    L.mla_set_impl(impl)
+
+    base = make_inputs(args.workload, "cpu" if args.workload in ("tiny",) else dev).to(dev)
+    kv_bytes = base.kv_bytes()
+    B, T, H = base.B, base.T, base.H
+    n_splits = args.n_splits if args.n_splits > 0 else (4 if args.workload == "tiny" else 0)
+    # rotate cache copies so that each step reads HBM, not L2
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    n_copies = max(2, -(-3 * l2 // max(base.kv_cache.numel(), 1)))
+    n_copies = min(n_copies, 64)
+    caches = [base.kv_cache] + [base.kv_cache.clone() for _ in range(n_copies - 1)]
+    out = torch.empty((B, T, H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, T, H), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        L.mla_decode_paged(base.q, caches[i % n_copies], base.kv_scale, base.block_table,
+                           base.seq_lens, n_splits, base.sm_scale, out, lse, stream)
+
+    resolved = L.mla_auto_splits(B, T, H, base.block_table.shape[1], 0) if n_splits == 0 else n_splits
+    chunk = L.mla_split_chunk_pages(base.block_table.shape[1], resolved)
+    n_eff = -(-base.block_table.shape[1] // chunk)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    for i in range(args.warmup):
+        step(i)
+    barrier()
+    assert L.mla_device_error() == 0
+
+    # ---- main timed region: exactly K steps ----
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(stream)
+        barrier()
+    ms_total = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    value = world * kv_bytes / (ms_step * 1e-3) / 1e9
+    steps_per_s = 1e3 / ms_step
+
+    # ---- the dominant kernel alone, with events recorded around it on its stream ----
+    kprof = min(args.steps, 2000)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(kprof)]
+    for a, b_ in evs:  # create the underlying CUDA events on this stream
+        a.record(stream)
+        b_.record(stream)
+    barrier()
+    for i, (a, b_) in enumerate(evs):
+        L.mla_profile_next_decode(a.cuda_event, b_.cuda_event)
+        step(i)
+    barrier()
+    kernel_ms = sorted(a.elapsed_time(b_) for a, b_ in evs)
+    k_avg_ms = sum(kernel_ms) / len(kernel_ms)
+    peak, peak_src = load_peaks()
+    achieved = kv_bytes / (k_avg_ms * 1e-3) / 1e9
+    family = {1: "simt", 2: "tcgen05"}.get(L.mla_last_decode_impl(), "unknown")
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": ncu_traffic(family, args.workload),
+                "peak_source": peak_src, "kernel": f"{family} split-KV decode",
+                "kernel_avg_us": round(k_avg_ms * 1e3, 2),
+                "kernel_p50_us": round(kernel_ms[len(kernel_ms) // 2] * 1e3, 2),
+                "frac_of_8TBps": round(achieved / HBM_NOMINAL_GBS, 4),
+                "algorithmic_bytes_per_launch": kv_bytes}
+
+    # ---- end to end through the C ABI with host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        hq = base.q.cpu().pin_memory()
+        hbt = base.block_table.cpu().pin_memory()
+        hsl = base.seq_lens.cpu().pin_memory()
+        hks = base.kv_scale.cpu().pin_memory()
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        dq, dbt, dsl, dks = (torch.empty_like(base.q), torch.empty_like(base.block_table),
+                             torch.empty_like(base.seq_lens), torch.empty_like(base.kv_scale))
+        ksteps = min(args.steps, 1000)
+
+        def e2e_step(i):
+            dq.copy_(hq, non_blocking=True)
+            dbt.copy_(hbt, non_blocking=True)
+            dsl.copy_(hsl, non_blocking=True)
+            dks.copy_(hks, non_blocking=True)
+            L.mla_decode_paged(dq, caches[i % n_copies], dks, dbt, dsl, n_splits, base.sm_scale,
+                               out, lse, stream)
+            hout.copy_(out, non_blocking=True)
+            hlse.copy_(lse, non_blocking=True)
+            stream.synchronize()
+
+        for i in range(3):
+            e2e_step(i)
+        barrier()
+        t0 = time.perf_counter()
+        for i in range(ksteps):
+            e2e_step(i)
+        barrier()
+        e2e_ms = (time.perf_counter() - t0) * 1e3 / ksteps
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        h2d = sum(x.numel() * x.element_size() for x in (hq, hbt, hsl, hks))
+        d2h = sum(x.numel() * x.element_size() for x in (hout, hlse))
+        e2e = {"value": round(world * kv_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+               "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": ksteps, "note": "pinned host q/block_table/seq_lens/kv_scale -> device, "
+               "decode, out+lse -> host, stream synchronised every step; the latent cache is "
+               "resident decode state"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(base, budget_s=15.0)
+
+    if rank == 0:
+        clocks = clk.summary()
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3fn KV x bf16 q, f32 accumulate", "data": "synthetic",
+            "config": {"workload": f"{args.workload}: {workload_description(args.workload)}",
+                       "page": 64, "kv_bytes_per_step": kv_bytes, "n_splits": n_eff,
+                       "chunk_pages": chunk, "l2": f"{n_copies} rotating cache copies "
+                       f"({n_copies * base.kv_cache.numel() / 1e6:.0f} MB > L2 {l2 / 1e6:.0f} MB)",
+                       "kernel_family": family},
+            "decode_steps_per_s": round(steps_per_s, 1),
+            "frac_of_8TBps": round(value / HBM_NOMINAL_GBS, 4),
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": args.steps * (1 + (1 if n_eff > 1 else 0)),
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def cpu_baseline(case, budget_s=15.0):
+    """The FP64 oracle as it stands, on this host's cores, over a bounded sample of
+    the same workload (whole requests, all heads), reported in the same unit."""
+    import numpy as np
+    import oracle
+    c = case.to("cpu")
+    # calibrate on the first request, then take as many requests as fit the budget
+    t0 = time.perf_counter()
+    oracle.decode(c.q[:1], c.kv_cache, c.kv_scale, c.block_table[:1], c.seq_lens[:1], c.sm_scale)
+    t1 = time.perf_counter() - t0
+    n_req = int(max(1, min(c.B, budget_s / max(t1, 1e-3) * max(os.cpu_count() or 1, 1) / 2)))
+    t0 = time.perf_counter()
+    _, _, threads = oracle.decode(c.q[:n_req], c.kv_cache, c.kv_scale, c.block_table[:n_req],
+                                  c.seq_lens[:n_req], c.sm_scale, return_threads=True)
+    dt = time.perf_counter() - t0
+    kvb = 576 * int(np.sum(c.lens[:n_req]))
+    return {"value": round(kvb / dt / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n_req} of {c.B} requests (all heads, full context), {dt:.2f} s",
+            "seconds": round(dt, 3)}
+
+
+def run_reference(args):
+    """Reference arm: the FP64 CPU oracle on the host cores, same metric and unit."""
+    import torch
+    import numpy as np
+    import oracle
+    from mla_latent_kv_fp8_gb300 import synth
+
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    case = synth.workload_case(args.workload, device="cpu")
+    c = case
+    # each step is a bounded sample: the first request's first n positions, all heads
+    budget_total = 120.0
+    per_step = budget_total / max(args.steps + args.warmup, 1)
+    t0 = time.perf_counter()
+    L0 = c.lens[0]
+    oracle.decode(c.q[:1], c.kv_cache, c.kv_scale, c.block_table[:1], c.seq_lens[:1], c.sm_scale)
+    t_full = time.perf_counter() - t0
+    n = int(max(64, min(L0, L0 * per_step / max(t_full, 1e-6))))
+    mask = np.zeros(L0, dtype=np.uint8)
+    mask[:n] = 1
+
+    def step():
+        return oracle.decode(c.q[:1], c.kv_cache, c.kv_scale, c.block_table[:1], c.seq_lens[:1],
+                             c.sm_scale, pos_mask=mask, return_threads=True)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    threads = 1
+    for _ in range(args.steps):
+        threads = step()[2]
+    dt = (time.perf_counter() - t0) / args.steps
+    kvb = 576 * n
+    value = kvb / dt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{args.workload}: {workload_description(args.workload)}",
+                       "sample_per_step": f"request 0, positions [0, {n}), all {c.H} heads"},
+            "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": threads,
+                             "kind": "oracle", "sample": f"request 0, first {n} positions per step"},
+            "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

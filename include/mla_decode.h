@@ -1,0 +1,182 @@
+/*
+ * mla_decode.h -- C ABI of the GB300 (sm_103a) MLA decode library.
+ *
+ * One operation and its merge step, from the blog post "Kimi K3 on AMD
+ * Instinct MI355X: vLLM serving ..." (three language editions):
+ *
+ *   - Model section: every MLA layer keeps a compressed KV history that grows
+ *     with the conversation; each new query attends over all of it.
+ *   - Section 1 "Cache", DCP paragraph: a history can be cut into shards; each
+ *     partial answer carries normalisation information (its log-sum-exp) and
+ *     the partial answers are merged with softmax weights.  The worked figure
+ *     24 layers x 142,000 positions x 576 FP8 bytes fixes one byte per latent
+ *     element and no per-position scale bytes.
+ *   - Section 4 "MLA": query heads attend independently; the history is split
+ *     into parallel partitions inside one GPU and the results are combined,
+ *     with the KV storage unchanged.
+ *   - Benchmark configuration section: FP8 KV cache.
+ *
+ * Conventions this library fixes where the post is silent:
+ *   - a cached position is 576 OCP E4M3FN codes; codes [0, 512) are the latent
+ *     (also the value vector), codes [512, 576) the rotated positional part;
+ *   - one fp32 scale for the whole cache: x = e4m3fn(code) * (*kv_scale);
+ *   - pages of 64 positions, addressed through a block table;
+ *   - seq_lens[b] counts the T new positions; query t sees positions
+ *     p < seq_lens[b] - T + 1 + t;
+ *   - lse is the natural log of sum_p exp(score_p), score_p including sm_scale.
+ *
+ * Threading and ownership: every call is asynchronous on the given CUDA
+ * stream (a cudaStream_t passed as void*; NULL is the legacy default stream)
+ * and never synchronises with the host.  The caller owns every tensor; the
+ * library never frees or retains caller pointers beyond the call.  Scratch
+ * memory for split partials is owned by the library, kept per (device,
+ * stream) and grown with stream-ordered allocation on first need.  Calls on
+ * one stream are ordered; calls on different streams use different scratch.
+ *
+ * Errors: every entry point validates its arguments on the host before any
+ * launch and returns a status; mla_last_error() gives a message for the last
+ * failing call of the calling thread.  Device kernels never trap: bounded
+ * waits and (in bounds-checking builds) index checks write a device error
+ * word that mla_device_error() reads.
+ */
+#ifndef MLA_DECODE_H_
+#define MLA_DECODE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MLA_OK = 0,
+    MLA_ERR_INVALID_ARG = 1,  /* null pointer, wrong rank/shape/dtype/stride   */
+    MLA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. dims != 576)   */
+    MLA_ERR_CUDA = 3,         /* a CUDA runtime call failed; see mla_last_error */
+    MLA_ERR_NO_MEMORY = 4,    /* scratch allocation failed                      */
+    MLA_ERR_DEVICE = 5        /* a kernel reported an error (mla_device_error)  */
+} mla_status_t;
+
+typedef enum {
+    MLA_DTYPE_BF16 = 1,
+    MLA_DTYPE_F32 = 2,
+    MLA_DTYPE_E4M3FN = 3,     /* raw OCP E4M3FN codes, one byte each */
+    MLA_DTYPE_I32 = 4
+} mla_dtype_t;
+
+/* A strided view of device memory.  Strides are in elements.  This is the
+ * library's own descriptor (not DLPack); unused trailing dims are ignored. */
+typedef struct {
+    void *data;
+    int64_t shape[5];
+    int64_t stride[5];
+    int32_t ndim;
+    int32_t dtype;            /* an mla_dtype_t */
+} mla_tensor_t;
+
+/* Kernel families behind mla_decode_paged (see mla_set_impl). */
+typedef enum {
+    MLA_IMPL_AUTO = 0,        /* tensor-core kernel where supported, else CUDA-core */
+    MLA_IMPL_SIMT = 1,        /* CUDA-core split-KV kernel (FMA + shuffles)          */
+    MLA_IMPL_TCGEN05 = 2      /* tcgen05 tensor-core split-KV kernel                  */
+} mla_impl_t;
+
+/*
+ * mla_decode_paged -- MLA decode attention over a paged FP8 latent cache,
+ * split into n_splits parallel partitions of the history and merged by LSE.
+ *
+ *   q           bf16  [B, T, H, 576], device, innermost dim contiguous; the
+ *               absorbed, already-rotated query of each head.
+ *   kv_cache    e4m3fn [num_pages, 64, 576], device, fully contiguous; base
+ *               address 16-byte aligned.
+ *   kv_scale    device pointer to one fp32, the per-tensor dequantisation
+ *               scale (read on the device, so the call can be captured in a
+ *               CUDA graph while the scale changes).
+ *   block_table i32 [B, max_pages], device, innermost dim contiguous; entry
+ *               [b][j] is the physical page of positions 64j..64j+63 of
+ *               request b.  Only the first ceil(seq_lens[b] / 64) entries are
+ *               read; each must be in [0, num_pages).
+ *   seq_lens    i32 [B], device; history length of request b including its T
+ *               new positions; 0 (empty history) gives out = 0, lse = -inf;
+ *               must be <= 64 * max_pages, and >= T unless 0.
+ *   n_splits    > 0: use exactly this many history partitions per request;
+ *               0: choose automatically to fill every SM (mla_auto_splits).
+ *   sm_scale    softmax scale applied to q . x (e.g. 1/sqrt(192)).
+ *   out         bf16 [B, T, H, 512], device, contiguous, caller-allocated;
+ *               out = sum_p softmax_p * x_p[0:512], rounded to nearest even.
+ *   lse         fp32 [B, T, H], device, contiguous, or NULL; natural log of
+ *               the softmax normaliser (the merge weight of this answer).
+ *   stream      cudaStream_t as void*.
+ *
+ * Limits: H * T <= 128; dims fixed at 576 / 512; page size fixed at 64.
+ * Returns MLA_OK or an error status (nothing is launched on error).
+ * Out-of-range page ids and seq_lens are not checked on the host (that would
+ * need a synchronisation); bounds-checking builds flag them on the device.
+ */
+mla_status_t mla_decode_paged(const mla_tensor_t *q, const mla_tensor_t *kv_cache,
+                              const float *kv_scale, const mla_tensor_t *block_table,
+                              const mla_tensor_t *seq_lens, int32_t n_splits, float sm_scale,
+                              const mla_tensor_t *out, const mla_tensor_t *lse, void *stream);
+
+/*
+ * mla_merge_partials -- combine n_shards partial answers of the same rows by
+ * their normalisers (section 1, DCP merge):
+ *     lse = M + ln sum_s exp(lse_s - M),  M = max_s lse_s,
+ *     out = sum_s exp(lse_s - lse) * partial_out_s.
+ * Shards with lse_s = -inf weigh 0 and their partial_out is not read; rows
+ * whose every shard is -inf get out = 0, lse = -inf.
+ *
+ *   partial_out bf16 or fp32 [S, B, T, H, 512] (any rank >= 2 whose first dim
+ *               is S and last dim 512), device, contiguous.
+ *   partial_lse fp32 [S, B, T, H] (the same shape without the last dim).
+ *   n_shards    S (must equal partial_out->shape[0]); 1 <= S <= 4096.
+ *   out         bf16 [B, T, H, 512], device, contiguous.
+ *   lse         fp32 [B, T, H], device, contiguous, or NULL.
+ */
+mla_status_t mla_merge_partials(const mla_tensor_t *partial_out, const mla_tensor_t *partial_lse,
+                                int32_t n_shards, const mla_tensor_t *out,
+                                const mla_tensor_t *lse, void *stream);
+
+/* The automatic split count used when n_splits == 0: enough history
+ * partitions per request that B * splits fills every SM of the device
+ * (at least one full wave), with at least 2 pages (128 positions) each.
+ * Pure host function; sm_count <= 0 means "query the current device". */
+int32_t mla_auto_splits(int32_t B, int32_t T, int32_t H, int32_t max_pages, int32_t sm_count);
+
+/* Pages per partition for a given split count (even, so partitions are whole
+ * 128-position tiles), and the number of non-empty partitions per request. */
+int32_t mla_split_chunk_pages(int32_t max_pages, int32_t n_splits);
+
+/* Bytes of library scratch one mla_decode_paged call with these sizes uses
+ * (0 when n_splits resolves to 1). */
+size_t mla_decode_workspace_bytes(int32_t B, int32_t T, int32_t H, int32_t n_splits);
+
+/* Select the kernel family for subsequent mla_decode_paged calls in this
+ * process (all threads).  Returns the previous setting. */
+int32_t mla_set_impl(int32_t impl);
+
+/* Kernel family (MLA_IMPL_SIMT or MLA_IMPL_TCGEN05) that the calling thread's
+ * last successful mla_decode_paged call launched; 0 before any call. */
+int32_t mla_last_decode_impl(void);
+
+/* Synchronise `stream`, then read and clear the device error word of the
+ * current device: 0 means no kernel reported an error.  Codes: 1 a bounded
+ * wait timed out, 2 a page id out of range, 3 a seq_len out of range. */
+mla_status_t mla_device_error(int32_t *code, void *stream);
+
+/* Benchmark instrumentation: the next mla_decode_paged call made by the
+ * calling thread records ev_begin on its stream just before its split-KV
+ * kernel and ev_end just after that kernel (before the split combine).  The
+ * events are cudaEvent_t handles passed as void*; either may be NULL.  The
+ * request is one-shot and thread-local; it changes nothing else. */
+mla_status_t mla_profile_next_decode(void *ev_begin, void *ev_end);
+
+const char *mla_status_string(mla_status_t status);
+const char *mla_last_error(void);   /* thread-local; "" when none */
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_DECODE_H_ */

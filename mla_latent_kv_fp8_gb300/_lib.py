@@ -1,0 +1,170 @@
+"""ctypes binding of the C ABI in include/mla_decode.h (argument marshalling only).
+
+Every function here has the same name and argument order as the C entry point
+it wraps.  Tensors are torch tensors on the GPU; they are described to the
+library by pointer, shape and strides, and the library launches its own CUDA
+kernels on the given stream.  There is no fallback: if the compiled library
+is missing, importing this module fails with an error that says how to build it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmla_decode.so")
+
+MLA_OK = 0
+STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED", 3: "MLA_ERR_CUDA",
+          4: "MLA_ERR_NO_MEMORY", 5: "MLA_ERR_DEVICE"}
+IMPL_AUTO, IMPL_SIMT, IMPL_TCGEN05 = 0, 1, 2
+
+_DTYPES = {torch.bfloat16: 1, torch.float32: 2, torch.uint8: 3, torch.float8_e4m3fn: 3, torch.int32: 4}
+
+# Every symbol include/mla_decode.h declares.
+EXPORTS = ("mla_decode_paged", "mla_merge_partials", "mla_auto_splits", "mla_split_chunk_pages",
+           "mla_decode_workspace_bytes", "mla_set_impl", "mla_device_error", "mla_status_string",
+           "mla_last_error", "mla_profile_next_decode", "mla_last_decode_impl")
+
+
+class MlaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+class mla_tensor_t(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("shape", ctypes.c_int64 * 5),
+                ("stride", ctypes.c_int64 * 5), ("ndim", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with `python -c \"import __graft_entry__ as g; "
+                          f"g.build()\"` (nvcc, sm_103a)")
+    lib = ctypes.CDLL(path)
+    P, T = ctypes.c_void_p, ctypes.POINTER(mla_tensor_t)
+    lib.mla_decode_paged.argtypes = [T, T, P, T, T, ctypes.c_int32, ctypes.c_float, T, T, P]
+    lib.mla_decode_paged.restype = ctypes.c_int
+    lib.mla_merge_partials.argtypes = [T, T, ctypes.c_int32, T, T, P]
+    lib.mla_merge_partials.restype = ctypes.c_int
+    lib.mla_auto_splits.argtypes = [ctypes.c_int32] * 5
+    lib.mla_auto_splits.restype = ctypes.c_int32
+    lib.mla_split_chunk_pages.argtypes = [ctypes.c_int32, ctypes.c_int32]
+    lib.mla_split_chunk_pages.restype = ctypes.c_int32
+    lib.mla_decode_workspace_bytes.argtypes = [ctypes.c_int32] * 4
+    lib.mla_decode_workspace_bytes.restype = ctypes.c_size_t
+    lib.mla_set_impl.argtypes = [ctypes.c_int32]
+    lib.mla_set_impl.restype = ctypes.c_int32
+    lib.mla_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32), P]
+    lib.mla_device_error.restype = ctypes.c_int
+    lib.mla_last_decode_impl.argtypes = []
+    lib.mla_last_decode_impl.restype = ctypes.c_int32
+    lib.mla_profile_next_decode.argtypes = [P, P]
+    lib.mla_profile_next_decode.restype = ctypes.c_int
+    lib.mla_status_string.argtypes = [ctypes.c_int]
+    lib.mla_status_string.restype = ctypes.c_char_p
+    lib.mla_last_error.argtypes = []
+    lib.mla_last_error.restype = ctypes.c_char_p
+    return lib
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        _lib = load_library()
+    return _lib
+
+
+def describe(t: torch.Tensor | None):
+    """torch tensor -> mla_tensor_t (no copy; the tensor must outlive the call)."""
+    if t is None:
+        return None
+    if t.dim() > 5:
+        raise ValueError("at most 5 dims")
+    d = mla_tensor_t()
+    d.data = t.data_ptr()
+    for i in range(t.dim()):
+        d.shape[i] = t.shape[i]
+        d.stride[i] = t.stride(i)
+    d.ndim = t.dim()
+    d.dtype = _DTYPES.get(t.dtype, 0)
+    return d
+
+
+def _ref(d):
+    return ctypes.byref(d) if d is not None else None
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _check(status: int):
+    if status != MLA_OK:
+        raise MlaError(status, lib().mla_last_error().decode())
+
+
+def mla_decode_paged(q, kv_cache, kv_scale, block_table, seq_lens, n_splits, sm_scale, out,
+                     lse=None, stream=None):
+    """out[b,t,h] = softmax(q . x^T * sm_scale) . x[:, :512] over the paged FP8 history."""
+    dq, dkv, dbt, dsl, do, dl = (describe(q), describe(kv_cache), describe(block_table),
+                                 describe(seq_lens), describe(out), describe(lse))
+    _check(lib().mla_decode_paged(_ref(dq), _ref(dkv), ctypes.c_void_p(kv_scale.data_ptr()),
+                                  _ref(dbt), _ref(dsl), int(n_splits), float(sm_scale), _ref(do),
+                                  _ref(dl), _stream(stream)))
+
+
+def mla_merge_partials(partial_out, partial_lse, n_shards, out, lse=None, stream=None):
+    """Merge S partial answers [S, ..., 512] by their log-sum-exp normalisers."""
+    dpo, dpl, do, dl = describe(partial_out), describe(partial_lse), describe(out), describe(lse)
+    _check(lib().mla_merge_partials(_ref(dpo), _ref(dpl), int(n_shards), _ref(do), _ref(dl),
+                                    _stream(stream)))
+
+
+def mla_auto_splits(B, T, H, max_pages, sm_count=0):
+    return lib().mla_auto_splits(B, T, H, max_pages, sm_count)
+
+
+def mla_split_chunk_pages(max_pages, n_splits):
+    return lib().mla_split_chunk_pages(max_pages, n_splits)
+
+
+def mla_decode_workspace_bytes(B, T, H, n_splits):
+    return lib().mla_decode_workspace_bytes(B, T, H, n_splits)
+
+
+def mla_set_impl(impl: int) -> int:
+    return lib().mla_set_impl(impl)
+
+
+def mla_last_decode_impl() -> int:
+    return lib().mla_last_decode_impl()
+
+
+def mla_device_error(stream=None) -> int:
+    code = ctypes.c_int32(0)
+    _check(lib().mla_device_error(ctypes.byref(code), _stream(stream)))
+    return code.value
+
+
+def mla_profile_next_decode(ev_begin, ev_end):
+    """Record raw cudaEvent_t handles (ints) around the next decode kernel of this thread."""
+    _check(lib().mla_profile_next_decode(ctypes.c_void_p(ev_begin or 0), ctypes.c_void_p(ev_end or 0)))
+
+
+def mla_status_string(status: int) -> str:
+    return lib().mla_status_string(status).decode()
+
+
+def mla_last_error() -> str:
+    return lib().mla_last_error().decode()

@@ -1,0 +1,389 @@
+// mla_api.cu -- host side of the C ABI declared in include/mla_decode.h:
+// argument validation, split planning, library-owned scratch, kernel dispatch
+// and error reporting.  Everything here runs on the host; every step of the
+// attention itself runs in the CUDA kernels.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <utility>
+
+#include "../../include/mla_decode.h"
+#include "mla_internal.cuh"
+
+// The device error word written by kernels (bounded waits, bounds checks).
+__device__ int g_mla_device_error;
+
+namespace mla {
+
+cudaError_t launch_tc_decode(const DecodeParams& p, cudaStream_t stream, bool* handled);
+
+namespace {
+
+thread_local std::string t_last_error;
+thread_local cudaEvent_t t_prof_begin = nullptr;
+thread_local cudaEvent_t t_prof_end = nullptr;
+thread_local int t_last_impl = 0;
+std::atomic<int> g_impl{MLA_IMPL_AUTO};
+
+mla_status_t fail(mla_status_t st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return st;
+}
+
+mla_status_t cuda_fail(cudaError_t e, const char* what) {
+    cudaGetLastError();  // clear a sticky launch error so later calls are not blamed
+    return fail(MLA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// Per-device facts, filled once per device.
+struct DeviceInfo {
+    bool ready = false;
+    int sm_count = 0;
+    int* err_word = nullptr;
+};
+std::mutex g_dev_mu;
+DeviceInfo g_dev[64];
+
+mla_status_t device_info(DeviceInfo** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(MLA_ERR_UNSUPPORTED, "device ordinal %d >= 64", dev);
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        void* addr = nullptr;
+        e = cudaGetSymbolAddress(&addr, g_mla_device_error);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(device error word)");
+        d.err_word = static_cast<int*>(addr);
+        d.ready = true;
+    }
+    *out = &d;
+    return MLA_OK;
+}
+
+// Library-owned split scratch, one buffer per (device, stream), grown in
+// stream order so that a buffer is never released while a kernel still uses it.
+struct Scratch {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+};
+std::mutex g_ws_mu;
+std::map<std::pair<int, void*>, Scratch> g_ws;
+
+mla_status_t get_scratch(size_t need, cudaStream_t stream, void** out) {
+    *out = nullptr;
+    if (need == 0) return MLA_OK;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    Scratch& s = g_ws[{dev, static_cast<void*>(stream)}];
+    if (s.bytes < need) {
+        if (s.ptr) {
+            e = cudaFreeAsync(s.ptr, stream);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync(scratch)");
+            s.ptr = nullptr;
+            s.bytes = 0;
+        }
+        size_t grow = need + need / 4;
+        e = cudaMallocAsync(&s.ptr, grow, stream);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            s.ptr = nullptr;
+            return fail(MLA_ERR_NO_MEMORY, "cudaMallocAsync(%zu bytes) for split scratch: %s", grow,
+                        cudaGetErrorString(e));
+        }
+        s.bytes = grow;
+    }
+    *out = s.ptr;
+    return MLA_OK;
+}
+
+bool contiguous(const mla_tensor_t* t) {
+    int64_t expect = 1;
+    for (int i = t->ndim - 1; i >= 0; --i) {
+        if (t->shape[i] != 1 && t->stride[i] != expect) return false;
+        expect *= t->shape[i];
+    }
+    return true;
+}
+
+mla_status_t check_tensor(const mla_tensor_t* t, const char* name, int ndim, int dtype,
+                          bool need_contig, size_t align) {
+    if (!t) return fail(MLA_ERR_INVALID_ARG, "%s: null descriptor", name);
+    if (t->ndim != ndim) return fail(MLA_ERR_INVALID_ARG, "%s: rank %d, expected %d", name, t->ndim, ndim);
+    if (t->dtype != dtype) return fail(MLA_ERR_INVALID_ARG, "%s: dtype %d, expected %d", name, t->dtype, dtype);
+    for (int i = 0; i < ndim; ++i)
+        if (t->shape[i] < 0) return fail(MLA_ERR_INVALID_ARG, "%s: negative dim %d", name, i);
+    if (need_contig && !contiguous(t))
+        return fail(MLA_ERR_UNSUPPORTED, "%s: must be contiguous", name);
+    int64_t numel = 1;
+    for (int i = 0; i < ndim; ++i) numel *= t->shape[i];
+    if (numel > 0 && !t->data) return fail(MLA_ERR_INVALID_ARG, "%s: null data", name);
+    if (align > 1 && (reinterpret_cast<uintptr_t>(t->data) % align) != 0)
+        return fail(MLA_ERR_UNSUPPORTED, "%s: data must be %zu-byte aligned", name, align);
+    return MLA_OK;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+const char* mla_status_string(mla_status_t s) {
+    switch (s) {
+        case MLA_OK: return "MLA_OK";
+        case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
+        case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
+        case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+        case MLA_ERR_NO_MEMORY: return "MLA_ERR_NO_MEMORY";
+        case MLA_ERR_DEVICE: return "MLA_ERR_DEVICE";
+    }
+    return "MLA_ERR_UNKNOWN";
+}
+
+const char* mla_last_error(void) { return t_last_error.c_str(); }
+
+int32_t mla_set_impl(int32_t impl) { return g_impl.exchange(impl); }
+
+int32_t mla_last_decode_impl(void) { return t_last_impl; }
+
+int32_t mla_auto_splits(int32_t B, int32_t T, int32_t H, int32_t max_pages, int32_t sm_count) {
+    (void)T;
+    (void)H;
+    if (B <= 0 || max_pages <= 2) return 1;
+    if (sm_count <= 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            sm_count = 148;
+        }
+    }
+    // One full wave of (request, partition) units, partitions of >= 2 pages.
+    int64_t s = ceil_div(sm_count, B);
+    const int64_t most = ceil_div(max_pages, 2);
+    if (s > most) s = most;
+    if (s < 1) s = 1;
+    // Snap to the count that equal even-page chunks actually produce.
+    const int64_t chunk = mla_split_chunk_pages(max_pages, (int32_t)s);
+    return (int32_t)ceil_div(max_pages, chunk);
+}
+
+int32_t mla_split_chunk_pages(int32_t max_pages, int32_t n_splits) {
+    if (max_pages <= 0) return 2;
+    if (n_splits < 1) n_splits = 1;
+    int64_t chunk = ceil_div(max_pages, n_splits);
+    chunk += chunk & 1;
+    return (int32_t)(chunk < 2 ? 2 : chunk);
+}
+
+size_t mla_decode_workspace_bytes(int32_t B, int32_t T, int32_t H, int32_t n_splits) {
+    if (n_splits <= 1 || B <= 0) return 0;
+    const size_t rows = (size_t)B * T * H;
+    const size_t out_bytes = (size_t)n_splits * rows * kDv * sizeof(float);
+    const size_t lse_bytes = (size_t)n_splits * rows * sizeof(float);
+    return ((out_bytes + 255) & ~size_t(255)) + lse_bytes;
+}
+
+mla_status_t mla_device_error(int32_t* code, void* stream) {
+    if (!code) return fail(MLA_ERR_INVALID_ARG, "code: null pointer");
+    DeviceInfo* d = nullptr;
+    mla_status_t st = device_info(&d);
+    if (st != MLA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    int v = 0;
+    e = cudaMemcpy(&v, d->err_word, sizeof v, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(device error word)");
+    if (v != 0) {
+        const int zero = 0;
+        e = cudaMemcpy(d->err_word, &zero, sizeof zero, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(clear device error word)");
+    }
+    *code = v;
+    return MLA_OK;
+}
+
+mla_status_t mla_decode_paged(const mla_tensor_t* q, const mla_tensor_t* kv_cache,
+                              const float* kv_scale, const mla_tensor_t* block_table,
+                              const mla_tensor_t* seq_lens, int32_t n_splits, float sm_scale,
+                              const mla_tensor_t* out, const mla_tensor_t* lse, void* stream) {
+    t_last_error.clear();
+    mla_status_t st;
+    if ((st = check_tensor(q, "q", 4, MLA_DTYPE_BF16, true, 16)) != MLA_OK) return st;
+    const int64_t B = q->shape[0], T = q->shape[1], H = q->shape[2];
+    if (q->shape[3] != kDqk) return fail(MLA_ERR_UNSUPPORTED, "q: last dim %lld, only 576 is supported", (long long)q->shape[3]);
+    if (T < 1 || H < 1) return fail(MLA_ERR_INVALID_ARG, "q: T and H must be >= 1");
+    if (H * T > kMaxRows) return fail(MLA_ERR_UNSUPPORTED, "H*T = %lld exceeds %d", (long long)(H * T), kMaxRows);
+    if ((st = check_tensor(kv_cache, "kv_cache", 3, MLA_DTYPE_E4M3FN, true, 16)) != MLA_OK) return st;
+    if (kv_cache->shape[1] != kPage || kv_cache->shape[2] != kDqk)
+        return fail(MLA_ERR_UNSUPPORTED, "kv_cache: must be [num_pages, 64, 576]");
+    if (!kv_scale) return fail(MLA_ERR_INVALID_ARG, "kv_scale: null pointer");
+    if ((st = check_tensor(block_table, "block_table", 2, MLA_DTYPE_I32, false, 4)) != MLA_OK) return st;
+    if (block_table->shape[0] != B) return fail(MLA_ERR_INVALID_ARG, "block_table: first dim must be B");
+    const int64_t max_pages = block_table->shape[1];
+    if (block_table->stride[1] != 1 || block_table->stride[0] < max_pages)
+        return fail(MLA_ERR_UNSUPPORTED, "block_table: rows must be contiguous");
+    if ((st = check_tensor(seq_lens, "seq_lens", 1, MLA_DTYPE_I32, true, 4)) != MLA_OK) return st;
+    if (seq_lens->shape[0] != B) return fail(MLA_ERR_INVALID_ARG, "seq_lens: must have B entries");
+    if ((st = check_tensor(out, "out", 4, MLA_DTYPE_BF16, true, 16)) != MLA_OK) return st;
+    if (out->shape[0] != B || out->shape[1] != T || out->shape[2] != H || out->shape[3] != kDv)
+        return fail(MLA_ERR_INVALID_ARG, "out: must be [B, T, H, 512]");
+    if (lse) {
+        if ((st = check_tensor(lse, "lse", 3, MLA_DTYPE_F32, true, 4)) != MLA_OK) return st;
+        if (lse->shape[0] != B || lse->shape[1] != T || lse->shape[2] != H)
+            return fail(MLA_ERR_INVALID_ARG, "lse: must be [B, T, H]");
+    }
+    if (n_splits < 0) return fail(MLA_ERR_INVALID_ARG, "n_splits must be >= 0");
+    if (max_pages < 1 && B > 0) return fail(MLA_ERR_INVALID_ARG, "block_table: needs >= 1 column");
+    if (max_pages > (1 << 24)) return fail(MLA_ERR_UNSUPPORTED, "block_table: more than 2^24 pages per request");
+    if (B > 65535) return fail(MLA_ERR_UNSUPPORTED, "B > 65535");
+    if (B == 0) return MLA_OK;
+
+    DeviceInfo* dev = nullptr;
+    if ((st = device_info(&dev)) != MLA_OK) return st;
+
+    const int32_t req = n_splits > 0 ? n_splits
+                                     : mla_auto_splits((int32_t)B, (int32_t)T, (int32_t)H,
+                                                       (int32_t)max_pages, dev->sm_count);
+    const int32_t chunk = mla_split_chunk_pages((int32_t)max_pages, req);
+    const int32_t n_eff = (int32_t)ceil_div(max_pages, chunk);
+
+    DecodeParams p{};
+    p.q = static_cast<const uint16_t*>(q->data);
+    p.kv = static_cast<const uint8_t*>(kv_cache->data);
+    p.kv_scale = kv_scale;
+    p.block_table = static_cast<const int32_t*>(block_table->data);
+    p.seq_lens = static_cast<const int32_t*>(seq_lens->data);
+    p.bt_stride = block_table->stride[0];
+    p.num_pages = kv_cache->shape[0];
+    p.B = (int)B;
+    p.T = (int)T;
+    p.H = (int)H;
+    p.max_pages = (int)max_pages;
+    p.n_splits = n_eff;
+    p.chunk_pages = chunk;
+    p.sm_scale_log2 = sm_scale * kLog2e;
+    p.out = static_cast<uint16_t*>(out->data);
+    p.lse = lse ? static_cast<float*>(lse->data) : nullptr;
+    p.err = dev->err_word;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (n_eff > 1) {
+        void* ws = nullptr;
+        const size_t need = mla_decode_workspace_bytes((int32_t)B, (int32_t)T, (int32_t)H, n_eff);
+        if ((st = get_scratch(need, s, &ws)) != MLA_OK) return st;
+        const size_t out_bytes = (size_t)n_eff * B * T * H * kDv * sizeof(float);
+        p.part_out = static_cast<float*>(ws);
+        p.part_lse = reinterpret_cast<float*>(static_cast<char*>(ws) + ((out_bytes + 255) & ~size_t(255)));
+    }
+
+    const int impl = g_impl.load();
+    cudaError_t e = cudaSuccess;
+    bool handled = false;
+    cudaEvent_t ev_begin = t_prof_begin, ev_end = t_prof_end;
+    t_prof_begin = t_prof_end = nullptr;
+    if (ev_begin && (e = cudaEventRecord(ev_begin, s)) != cudaSuccess)
+        return cuda_fail(e, "cudaEventRecord(profile begin)");
+    if (impl == MLA_IMPL_AUTO || impl == MLA_IMPL_TCGEN05) {
+        e = launch_tc_decode(p, s, &handled);
+        if (e != cudaSuccess) return cuda_fail(e, "tcgen05 decode launch");
+        if (!handled && impl == MLA_IMPL_TCGEN05)
+            return fail(MLA_ERR_UNSUPPORTED, "tcgen05 kernel does not support this shape");
+    }
+    if (!handled) {
+        e = launch_simt_decode(p, s);
+        if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    }
+    t_last_impl = handled ? MLA_IMPL_TCGEN05 : MLA_IMPL_SIMT;
+    if (ev_end && (e = cudaEventRecord(ev_end, s)) != cudaSuccess)
+        return cuda_fail(e, "cudaEventRecord(profile end)");
+    if (n_eff > 1) {
+        MergeParams m{};
+        m.part_out = p.part_out;
+        m.part_lse = p.part_lse;
+        m.S = n_eff;
+        m.rows = B * T * H;
+        m.in_bf16 = 0;
+        m.out = p.out;
+        m.lse = p.lse;
+        m.pdl = 1;
+        e = launch_merge(m, s);
+        if (e != cudaSuccess) return cuda_fail(e, "split combine launch");
+    }
+    return MLA_OK;
+}
+
+mla_status_t mla_profile_next_decode(void* ev_begin, void* ev_end) {
+    t_prof_begin = static_cast<cudaEvent_t>(ev_begin);
+    t_prof_end = static_cast<cudaEvent_t>(ev_end);
+    return MLA_OK;
+}
+
+mla_status_t mla_merge_partials(const mla_tensor_t* partial_out, const mla_tensor_t* partial_lse,
+                                int32_t n_shards, const mla_tensor_t* out, const mla_tensor_t* lse,
+                                void* stream) {
+    t_last_error.clear();
+    if (!partial_out || !partial_lse || !out)
+        return fail(MLA_ERR_INVALID_ARG, "partial_out, partial_lse and out are required");
+    const int nd = partial_out->ndim;
+    if (nd < 2 || nd > 5) return fail(MLA_ERR_INVALID_ARG, "partial_out: rank must be 2..5");
+    const int dt = partial_out->dtype;
+    if (dt != MLA_DTYPE_BF16 && dt != MLA_DTYPE_F32)
+        return fail(MLA_ERR_INVALID_ARG, "partial_out: dtype must be bf16 or fp32");
+    mla_status_t st;
+    if ((st = check_tensor(partial_out, "partial_out", nd, dt, true, 16)) != MLA_OK) return st;
+    if (partial_out->shape[nd - 1] != kDv) return fail(MLA_ERR_UNSUPPORTED, "partial_out: last dim must be 512");
+    if (n_shards < 1 || n_shards > 4096 || partial_out->shape[0] != n_shards)
+        return fail(MLA_ERR_INVALID_ARG, "n_shards must equal partial_out.shape[0] and lie in [1, 4096]");
+    if ((st = check_tensor(partial_lse, "partial_lse", nd - 1, MLA_DTYPE_F32, true, 4)) != MLA_OK) return st;
+    int64_t rows = 1;
+    for (int i = 0; i < nd - 1; ++i)
+        if (partial_lse->shape[i] != partial_out->shape[i])
+            return fail(MLA_ERR_INVALID_ARG, "partial_lse: shape must be partial_out.shape[:-1]");
+    for (int i = 1; i < nd - 1; ++i) rows *= partial_out->shape[i];
+    if ((st = check_tensor(out, "out", nd - 1, MLA_DTYPE_BF16, true, 16)) != MLA_OK) return st;
+    for (int i = 1; i < nd; ++i)
+        if (out->shape[i - 1] != partial_out->shape[i])
+            return fail(MLA_ERR_INVALID_ARG, "out: shape must be partial_out.shape[1:]");
+    if (lse) {
+        if (nd - 2 == 0) return fail(MLA_ERR_INVALID_ARG, "lse: rank-0 output not supported; pass NULL");
+        if ((st = check_tensor(lse, "lse", nd - 2, MLA_DTYPE_F32, true, 4)) != MLA_OK) return st;
+        for (int i = 1; i < nd - 1; ++i)
+            if (lse->shape[i - 1] != partial_out->shape[i])
+                return fail(MLA_ERR_INVALID_ARG, "lse: shape must be partial_out.shape[1:-1]");
+    }
+    if (rows == 0) return MLA_OK;
+    MergeParams m{};
+    m.part_out = partial_out->data;
+    m.part_lse = static_cast<const float*>(partial_lse->data);
+    m.S = n_shards;
+    m.rows = rows;
+    m.in_bf16 = dt == MLA_DTYPE_BF16;
+    m.out = static_cast<uint16_t*>(out->data);
+    m.lse = lse ? static_cast<float*>(lse->data) : nullptr;
+    m.pdl = 0;
+    cudaError_t e = launch_merge(m, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+    return MLA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,187 @@
+// mla_merge.cu -- merge of partial attention answers by their log-sum-exp.
+//
+// "Kimi K3 on AMD Instinct MI355X" post, section 1 (DCP paragraph): each
+// partial answer over a part of the history carries normalisation information
+// so that the merge weighs the parts correctly.  With lse_s the natural-log
+// normaliser of part s:
+//     lse = M + ln sum_s exp(lse_s - M),   M = max_s lse_s
+//     out = sum_s exp(lse_s - lse) * o_s
+// Parts with lse_s = -inf weigh exactly 0 and are not read.
+//
+// Two kernels:
+//   * few parts (S <= 32): one warp per (row, 128 value dims); lane s holds
+//     lse_s, the normaliser is a shuffle reduction, each lane streams 4 dims
+//     of every part with one vector load per part;
+//   * many parts (S > 32, the in-GPU split combine of one long request): one
+//     CTA per (row, 32 value dims); the eight warps split the parts, each lane
+//     owns one dim, and the warps' sums meet in shared memory.
+#include <cuda_bf16.h>
+
+#include "mla_internal.cuh"
+
+namespace mla {
+namespace {
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ void wait_for_producer(int pdl) {
+    if (pdl) asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+template <bool kBf16In>
+__device__ __forceinline__ float4 load4(const void* base, int64_t idx) {
+    if constexpr (kBf16In) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + idx);
+        return make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xffff0000u),
+                           __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xffff0000u));
+    } else {
+        return *reinterpret_cast<const float4*>(static_cast<const float*>(base) + idx);
+    }
+}
+
+template <bool kBf16In>
+__device__ __forceinline__ float load1(const void* base, int64_t idx) {
+    if constexpr (kBf16In) {
+        return __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t*>(base)[idx]) << 16);
+    } else {
+        return static_cast<const float*>(base)[idx];
+    }
+}
+
+template <bool kBf16In>
+__global__ void __launch_bounds__(256) merge_warp_kernel(MergeParams p) {
+    wait_for_producer(p.pdl);
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (gw >= p.rows * 4) return;
+    const int64_t row = gw >> 2;
+    const int chunk = (int)(gw & 3);
+    const int64_t col = (int64_t)chunk * 128 + lane * 4;
+
+    const float ls = (lane < p.S) ? p.part_lse[(int64_t)lane * p.rows + row] : -INFINITY;
+    const float M = warp_max(ls);
+    uint16_t* dst = p.out + row * kDv + col;
+    if (M == -INFINITY) {
+        *reinterpret_cast<uint2*>(dst) = make_uint2(0u, 0u);
+        if (chunk == 0 && lane == 0 && p.lse) p.lse[row] = -INFINITY;
+        return;
+    }
+    const float e = (ls == -INFINITY) ? 0.f : exp2f((ls - M) * kLog2e);
+    const float sum = warp_sum(e);
+    const float w = e / sum;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < p.S; ++s) {
+        const float ws = __shfl_sync(0xffffffffu, w, s);
+        if (ws == 0.f) continue;
+        const float4 v = load4<kBf16In>(p.part_out, ((int64_t)s * p.rows + row) * kDv + col);
+        acc.x = fmaf(ws, v.x, acc.x);
+        acc.y = fmaf(ws, v.y, acc.y);
+        acc.z = fmaf(ws, v.z, acc.z);
+        acc.w = fmaf(ws, v.w, acc.w);
+    }
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+    *reinterpret_cast<uint2*>(dst) =
+        make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+    if (chunk == 0 && lane == 0 && p.lse) p.lse[row] = M + logf(sum);
+}
+
+template <bool kBf16In>
+__global__ void __launch_bounds__(256) merge_cta_kernel(MergeParams p) {
+    wait_for_producer(p.pdl);
+    __shared__ float red[8];
+    __shared__ float part[8][32];
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int64_t row = blockIdx.x >> 4;
+    const int col = (blockIdx.x & 15) * 32 + lane;
+
+    float mx = -INFINITY;
+    for (int s = tid; s < p.S; s += 256) mx = fmaxf(mx, p.part_lse[(int64_t)s * p.rows + row]);
+    mx = warp_max(mx);
+    if (lane == 0) red[wid] = mx;
+    __syncthreads();
+    float M = red[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) M = fmaxf(M, red[i]);
+    __syncthreads();
+    if (M == -INFINITY) {
+        if (wid == 0) {
+            p.out[row * kDv + col] = 0;
+            if (blockIdx.x % 16 == 0 && lane == 0 && p.lse) p.lse[row] = -INFINITY;
+        }
+        return;
+    }
+    float sm = 0.f;
+    for (int s = tid; s < p.S; s += 256) {
+        const float ls = p.part_lse[(int64_t)s * p.rows + row];
+        if (ls != -INFINITY) sm += exp2f((ls - M) * kLog2e);
+    }
+    sm = warp_sum(sm);
+    if (lane == 0) red[wid] = sm;
+    __syncthreads();
+    float sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sum += red[i];
+    const float lse_out = M + logf(sum);
+
+    float acc = 0.f;
+#pragma unroll 4
+    for (int s = wid; s < p.S; s += 8) {
+        const float ls = p.part_lse[(int64_t)s * p.rows + row];
+        if (ls == -INFINITY) continue;
+        const float w = exp2f((ls - lse_out) * kLog2e);
+        acc = fmaf(w, load1<kBf16In>(p.part_out, ((int64_t)s * p.rows + row) * kDv + col), acc);
+    }
+    part[wid][lane] = acc;
+    __syncthreads();
+    if (wid == 0) {
+        float t = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) t += part[i][lane];
+        __nv_bfloat16 v = __float2bfloat16_rn(t);
+        p.out[row * kDv + col] = *reinterpret_cast<uint16_t*>(&v);
+        if ((blockIdx.x & 15) == 0 && lane == 0 && p.lse) p.lse[row] = lse_out;
+    }
+}
+
+template <typename K>
+cudaError_t launch_with_pdl(K kernel, dim3 grid, dim3 block, cudaStream_t stream,
+                            const MergeParams& p) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = p.pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
+}  // namespace
+
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
+    if (p.rows == 0) return cudaSuccess;
+    if (p.S <= 32) {
+        const int64_t warps = p.rows * 4;
+        const dim3 grid((unsigned)((warps + 7) / 8));
+        return p.in_bf16 ? launch_with_pdl(merge_warp_kernel<true>, grid, dim3(256), stream, p)
+                         : launch_with_pdl(merge_warp_kernel<false>, grid, dim3(256), stream, p);
+    }
+    const dim3 grid((unsigned)(p.rows * 16));
+    return p.in_bf16 ? launch_with_pdl(merge_cta_kernel<true>, grid, dim3(256), stream, p)
+                     : launch_with_pdl(merge_cta_kernel<false>, grid, dim3(256), stream, p);
+}
+
+}  // namespace mla

@@ -29,7 +29,8 @@ D_QK = 576
 D_V = 512
 FP8_MAX = 448.0
 SM_SCALE = 1.0 / math.sqrt(192.0)
-_CHUNK = 8192  # positions per generation chunk
+_CHUNK = 8192  # positions per generation chunk (CPU)
+_CHUNK_CUDA = 65536  # positions per generation chunk (GPU)
 
 
 @dataclass
@@ -93,11 +94,12 @@ def _latent_codes(seed, lens_padded, device, scale=None):
 
     Two passes over the same seed-addressed chunks: amax first (unless a scale
     is supplied), then quantisation.  Returns (list of uint8 tensors, scale)."""
+    chunk = _CHUNK_CUDA if device.type == "cuda" else _CHUNK
     if scale is None:
         amax = 0.0
         for b, L in enumerate(lens_padded):
-            for c0 in range(0, L, _CHUNK):
-                n = min(_CHUNK, L - c0) * D_QK
+            for c0 in range(0, L, chunk):
+                n = min(chunk, L - c0) * D_QK
                 x = _normal_chunk((seed, 7, b, c0), n, device)
                 amax = max(amax, float(x.abs().max()))
         scale = np.float32(amax) / np.float32(FP8_MAX)
@@ -106,8 +108,8 @@ def _latent_codes(seed, lens_padded, device, scale=None):
     st = torch.tensor(float(scale), dtype=torch.float32, device=device)
     for b, L in enumerate(lens_padded):
         out = torch.empty((L, D_QK), dtype=torch.uint8, device=device)
-        for c0 in range(0, L, _CHUNK):
-            m = min(_CHUNK, L - c0)
+        for c0 in range(0, L, chunk):
+            m = min(chunk, L - c0)
             x = _normal_chunk((seed, 7, b, c0), m * D_QK, device)
             y = torch.clamp(x / st, -FP8_MAX, FP8_MAX).to(torch.float8_e4m3fn)
             out[c0:c0 + m] = y.view(torch.uint8).view(m, D_QK)

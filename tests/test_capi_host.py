@@ -1,0 +1,154 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every symbol the header declares, plans splits as documented and rejects bad
+arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from mla_latent_kv_fp8_gb300 import build
+    build.build()
+    from mla_latent_kv_fp8_gb300 import _lib
+    return _lib
+
+
+def _declared_functions():
+    names = []
+    inc = os.path.join(ROOT, "include")
+    for f in sorted(os.listdir(inc)):
+        if f.endswith(".h"):
+            src = open(os.path.join(inc, f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"\b(mla_[a-z_0-9]+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_symbol(L):
+    lib = L.lib()
+    declared = _declared_functions()
+    assert "mla_decode_paged" in declared and "mla_merge_partials" in declared
+    for name in declared:
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+    assert set(L.EXPORTS) <= set(declared)
+
+
+def test_status_strings(L):
+    assert L.mla_status_string(0) == "MLA_OK"
+    assert L.mla_status_string(2) == "MLA_ERR_UNSUPPORTED"
+    assert L.mla_status_string(99) == "MLA_ERR_UNKNOWN"
+
+
+@pytest.mark.parametrize("B,max_pages,sm,expect", [
+    (8, 512, 152, 19),      # 8 requests x 32K: one wave of 152 units
+    (1, 6144, 152, 147),    # one request x 393K: >= SM count partitions
+    (1, 16, 152, 8),        # short history: partitions of >= 2 pages
+    (1, 2, 152, 1),
+    (200, 100, 152, 1),     # more requests than SMs: no split
+])
+def test_auto_splits(L, B, max_pages, sm, expect):
+    s = L.mla_auto_splits(B, 1, 12, max_pages, sm)
+    assert s == expect
+    chunk = L.mla_split_chunk_pages(max_pages, s)
+    assert chunk % 2 == 0 and chunk >= 2
+    assert -(-max_pages // chunk) == s  # every partition non-empty at full length
+
+
+def test_workspace_bytes(L):
+    assert L.mla_decode_workspace_bytes(8, 1, 12, 1) == 0
+    n = L.mla_decode_workspace_bytes(8, 1, 12, 19)
+    assert n >= 19 * 8 * 12 * 513 * 4
+
+
+def _desc(shape, dtype_code, ptr=0x10000):
+    d = L_mod().mla_tensor_t()
+    d.data = ptr
+    st = 1
+    strides = []
+    for s in reversed(shape):
+        strides.append(st)
+        st *= s
+    strides.reverse()
+    for i, (s, k) in enumerate(zip(shape, strides)):
+        d.shape[i] = s
+        d.stride[i] = k
+    d.ndim = len(shape)
+    d.dtype = dtype_code
+    return d
+
+
+def L_mod():
+    from mla_latent_kv_fp8_gb300 import _lib
+    return _lib
+
+
+def _call_decode(L, q, kv, bt, sl, out, lse, n_splits=0, scale_ptr=0x20000):
+    lib = L.lib()
+    ref = lambda d: ctypes.byref(d) if d is not None else None  # noqa: E731
+    return lib.mla_decode_paged(ref(q), ref(kv), ctypes.c_void_p(scale_ptr), ref(bt), ref(sl),
+                                n_splits, 0.07, ref(out), ref(lse), None)
+
+
+def _good(B=2, T=1, H=12, mp=4, npages=8):
+    return dict(q=_desc([B, T, H, 576], 1), kv=_desc([npages, 64, 576], 3), bt=_desc([B, mp], 4),
+                sl=_desc([B], 4), out=_desc([B, T, H, 512], 1), lse=_desc([B, T, H], 2))
+
+
+@pytest.mark.parametrize("mutate,status", [
+    (lambda a: a.update(q=None), 1),
+    (lambda a: setattr(a["q"], "dtype", 2), 1),
+    (lambda a: a.update(q=_desc([2, 1, 12, 512], 1)), 2),      # dims other than 576
+    (lambda a: a.update(q=_desc([2, 2, 96, 576], 1),
+                        out=_desc([2, 2, 96, 512], 1), lse=_desc([2, 2, 96], 2)), 2),  # H*T > 128
+    (lambda a: a.update(kv=_desc([8, 32, 576], 3)), 2),         # page size 32
+    (lambda a: a.update(bt=_desc([3, 4], 4)), 1),
+    (lambda a: a.update(sl=_desc([2], 2)), 1),
+    (lambda a: a.update(out=_desc([2, 1, 12, 576], 1)), 1),
+    (lambda a: a.update(lse=_desc([2, 1, 11], 2)), 1),
+    (lambda a: setattr(a["q"], "data", 0x10008), 2),           # misaligned q
+    (lambda a: a["q"].stride.__setitem__(3, 2), 2),            # non-contiguous q
+])
+def test_decode_rejects_bad_arguments_on_host(L, mutate, status):
+    a = _good()
+    mutate(a)
+    st = _call_decode(L, a["q"], a["kv"], a["bt"], a["sl"], a["out"], a["lse"])
+    assert st == status, L.mla_last_error()
+    assert L.mla_last_error() != ""
+
+
+def test_decode_rejects_negative_splits_and_null_scale(L):
+    a = _good()
+    assert _call_decode(L, a["q"], a["kv"], a["bt"], a["sl"], a["out"], a["lse"], n_splits=-1) == 1
+    assert _call_decode(L, a["q"], a["kv"], a["bt"], a["sl"], a["out"], a["lse"], scale_ptr=0) == 1
+
+
+def test_empty_batch_is_a_no_op(L):
+    a = _good(B=0)
+    assert _call_decode(L, a["q"], a["kv"], a["bt"], a["sl"], a["out"], a["lse"]) == 0
+
+
+def test_merge_rejects_bad_arguments_on_host(L):
+    lib = L.lib()
+    po, pl = _desc([4, 3, 512], 2), _desc([4, 3], 2)
+    out, lse = _desc([3, 512], 1), _desc([3], 2)
+    r = ctypes.byref
+    assert lib.mla_merge_partials(r(po), r(pl), 5, r(out), r(lse), None) == 1      # n_shards mismatch
+    assert lib.mla_merge_partials(r(po), r(_desc([4, 2], 2)), 4, r(out), r(lse), None) == 1
+    assert lib.mla_merge_partials(r(_desc([4, 3, 256], 2)), r(pl), 4, r(_desc([3, 256], 1)),
+                                  r(lse), None) == 2
+    assert lib.mla_merge_partials(r(_desc([4, 3, 512], 4)), r(pl), 4, r(out), r(lse), None) == 1
+    assert lib.mla_merge_partials(r(po), r(pl), 4, r(_desc([3, 512], 2)), r(lse), None) == 1
+
+
+def test_binding_maps_torch_dtypes(L):
+    d = L.describe(torch.zeros(2, 3, dtype=torch.bfloat16))
+    assert d.ndim == 2 and d.dtype == 1 and d.shape[1] == 3 and d.stride[0] == 3
+    assert L.describe(torch.zeros(1, dtype=torch.float8_e4m3fn)).dtype == 3
+    assert L.describe(torch.zeros(1, dtype=torch.int32)).dtype == 4
+    assert L.describe(None) is None

@@ -1,0 +1,247 @@
+"""GPU parity: the CUDA path (through the C ABI) against the FP64 oracle on the
+same seeded bytes, element by element, within the stated tolerances.
+
+Reduced-size cases compare every output; full-size workloads (the shapes the
+benchmark times, in the same launch configuration) compare sampled rows that
+the oracle computes one by one.  Output buffers are filled with NaN first so
+that an unwritten element fails."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mla_latent_kv_fp8_gb300 import synth
+from tests.parity import assert_parity
+
+pytestmark = pytest.mark.gpu
+
+IMPLS = {"simt": 1, "tcgen05": 2}
+
+
+@pytest.fixture(scope="module")
+def L():
+    from mla_latent_kv_fp8_gb300 import build
+    build.build()
+    from mla_latent_kv_fp8_gb300 import _lib
+    _lib.lib()
+    return _lib
+
+
+@pytest.fixture(params=sorted(IMPLS))
+def impl(request, L):
+    prev = L.mla_set_impl(IMPLS[request.param])
+    yield request.param
+    L.mla_set_impl(prev)
+
+
+def run(L, case, n_splits=0, with_lse=True, stream=None):
+    B, T, H = case.q.shape[:3]
+    out = torch.full((B, T, H, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, T, H), float("nan"), dtype=torch.float32, device="cuda") if with_lse else None
+    L.mla_decode_paged(case.q, case.kv_cache, case.kv_scale, case.block_table, case.seq_lens,
+                       n_splits, case.sm_scale, out, lse, stream)
+    torch.cuda.synchronize()
+    assert L.mla_device_error() == 0
+    return out, lse
+
+
+def supported(L, impl, case, n_splits=0):
+    """The tensor-core family declines shapes it does not cover; that is an error only
+    when it is the selected family."""
+    try:
+        return run(L, case, n_splits)
+    except L.MlaError as e:
+        if impl == "tcgen05" and e.status == 2:
+            pytest.skip(f"tcgen05 kernel does not cover this shape: {e}")
+        raise
+
+
+def oracle_full(case):
+    c = case.to("cpu")
+    return oracle.decode(c.q, c.kv_cache, c.kv_scale, c.block_table, c.seq_lens, c.sm_scale)
+
+
+def oracle_rows(case, reqs, heads):
+    """Oracle for the sampled requests/heads, on a compact identity-paged copy of
+    just those requests' pages (paging invariance is pinned separately)."""
+    reqs = list(reqs)
+    lens = [case.lens[b] for b in reqs]
+    pages = [(x + 63) // 64 for x in lens]
+    bt = case.block_table[reqs].cpu().numpy()
+    ids = np.concatenate([bt[i, :pages[i]] for i in range(len(reqs))]).astype(np.int64)
+    kv = case.kv_cache[torch.from_numpy(ids).to(case.kv_cache.device)].cpu()
+    bt_id = np.zeros((len(reqs), max(max(pages), 1)), dtype=np.int32)
+    off = 0
+    for i, p in enumerate(pages):
+        bt_id[i, :p] = np.arange(off, off + p)
+        off += p
+    q = case.q[reqs].cpu()
+    rm = np.zeros((len(reqs), case.T, case.H), dtype=np.uint8)
+    rm[:, :, heads] = 1
+    o, l = oracle.decode(q, kv, case.kv_scale.cpu(), torch.from_numpy(bt_id),
+                         torch.tensor(lens, dtype=torch.int32), case.sm_scale, row_mask=rm)
+    return o[:, :, heads], l[:, :, heads]
+
+
+# ----------------------------------------------------------------------------
+# Reduced sizes: every output against the oracle
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name,n_splits", [
+    ("tiny", 4), ("tiny", 1), ("tp8_batch", 0), ("tp8_batch", 1), ("tp8_batch", 3),
+    ("tp8_batch", 7), ("verify", 0), ("verify", 5), ("long", 0), ("long", 200),
+    ("ragged", 0), ("ragged", 9)])
+def test_reduced_workloads_match_oracle(L, impl, name, n_splits):
+    case = synth.workload_case(name, reduced=True)
+    out, lse = supported(L, impl, case.to("cuda"), n_splits)
+    ro, rl = oracle_full(case)
+    assert_parity(out, lse, ro, rl, what=f"{name}/{impl}/splits={n_splits}")
+
+
+@pytest.mark.parametrize("lens,H,T", [
+    ([1], 12, 1), ([64], 12, 1), ([65], 12, 1), ([128, 129, 127], 12, 1), ([4, 5, 68], 12, 4),
+    ([0, 300, 0], 12, 1), ([200], 1, 1), ([333, 17], 7, 3), ([260], 128, 1), ([190, 66], 32, 4),
+    ([517], 16, 8), ([1000], 96, 1)])
+def test_edge_shapes_match_oracle(L, impl, lens, H, T):
+    case = synth.make_decode_case(1000 + sum(lens) + H + T, lens, H, T, extra_pages=3)
+    for n_splits in (0, 1, 3):
+        out, lse = supported(L, impl, case.to("cuda"), n_splits)
+        ro, rl = oracle_full(case)
+        assert_parity(out, lse, ro, rl, what=f"lens={lens} H={H} T={T} splits={n_splits}")
+
+
+def test_more_splits_than_pages(L, impl):
+    case = synth.make_decode_case(77, [130, 5, 0], 12, 1)
+    out, lse = supported(L, impl, case.to("cuda"), 64)
+    ro, rl = oracle_full(case)
+    assert_parity(out, lse, ro, rl, what="64 splits over <= 3 pages")
+
+
+def test_unread_cache_bytes_do_not_leak(L, impl):
+    """NaN codes (0x7F) beyond seq_len inside the last page and in pages no request
+    references must not reach the output: only visible positions are read."""
+    lens = [70, 200, 1]
+    case = synth.make_decode_case(55, lens, 12, 1, extra_pages=4)
+    kv = case.kv_cache.clone()
+    bt = case.block_table.numpy()
+    for b, L_ in enumerate(lens):
+        last = (L_ - 1) // 64
+        kv[bt[b, last], L_ % 64 or 64:, :] = 0x7F
+    used = {int(bt[b, j]) for b, L_ in enumerate(lens) for j in range((L_ + 63) // 64)}
+    for pid in range(kv.shape[0]):
+        if pid not in used:
+            kv[pid] = 0x7F
+    case.kv_cache = kv
+    out, lse = supported(L, impl, case.to("cuda"), 0)
+    ro, rl = oracle_full(case)
+    assert_parity(out, lse, ro, rl, what="garbage outside the visible history")
+
+
+def test_lse_optional_and_deterministic(L, impl):
+    case = synth.workload_case("tp8_batch", reduced=True).to("cuda")
+    o1, l1 = supported(L, impl, case, 0)
+    o2, _ = run(L, case, 0, with_lse=False)
+    o3, l3 = run(L, case, 0)
+    assert torch.equal(o1, o2) and torch.equal(o1, o3) and torch.equal(l1, l3)
+
+
+def test_runs_on_a_side_stream(L, impl):
+    case = synth.workload_case("tiny").to("cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        out, lse = supported(L, impl, case, 4)
+    ro, rl = oracle_full(case)
+    assert_parity(out, lse, ro, rl, what="side stream")
+
+
+def test_dcp_shards_merge_to_unsharded(L, impl):
+    """Section 1 (DCP): 8 contiguous shards of one history, each decoded on its own
+    (out + lse), merged by mla_merge_partials, equal the unsharded oracle."""
+    sc = synth.make_sharded_case(3, 2, 96, 1200, 8)
+    outs, lses = [], []
+    for sh in sc.shards:
+        o, l = supported(L, impl, sh.to("cuda"), 0)
+        ro, rl = oracle_full(sh)
+        assert_parity(o, l, ro, rl, what="one shard")
+        outs.append(o)
+        lses.append(l)
+    po, pl = torch.stack(outs), torch.stack(lses)
+    out = torch.full(po.shape[1:], float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full(pl.shape[1:], float("nan"), dtype=torch.float32, device="cuda")
+    L.mla_merge_partials(po, pl, 8, out, lse)
+    torch.cuda.synchronize()
+    ro, rl = oracle_full(sc.full)
+    assert_parity(out, lse, ro, rl, what="merged shards vs unsharded")
+
+
+# ----------------------------------------------------------------------------
+# mla_merge_partials on its own
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("S", [1, 2, 8, 32, 33, 100])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_merge_partials_matches_oracle(L, S, dtype):
+    g = torch.Generator().manual_seed(S)
+    rows = (3, 5)
+    po = torch.randn((S, *rows, 512), generator=g).to(dtype)
+    pl = (torch.randn((S, *rows), generator=g) * 3).float()
+    drop = torch.rand((S, *rows), generator=g) < 0.3
+    pl[drop] = float("-inf")
+    pl[:, 0, 0] = float("-inf")  # a row with every shard empty
+    out = torch.full((*rows, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full(rows, float("nan"), dtype=torch.float32, device="cuda")
+    L.mla_merge_partials(po.cuda(), pl.cuda(), S, out, lse)
+    torch.cuda.synchronize()
+    ro, rl = oracle.merge(po.float().numpy().astype(np.float64), pl.numpy().astype(np.float64))
+    assert_parity(out, lse, ro, rl, what=f"merge S={S}")
+
+
+# ----------------------------------------------------------------------------
+# Full-size workloads, launched as the benchmark launches them; sampled rows
+# ----------------------------------------------------------------------------
+
+FULL = {
+    "tiny": ([0], list(range(12))),
+    "tp8_batch": ([0, 5, 7], [0, 6, 11]),
+    "verify": (None, [0, 11]),
+    "long": ([0], [0, 7]),
+    "ragged": (None, [3, 10]),
+}
+
+
+@pytest.mark.parametrize("name", sorted(FULL))
+def test_full_size_sampled_rows(L, impl, name):
+    case = synth.workload_case(name, device="cuda")
+    n_splits = 4 if name == "tiny" else 0
+    out, lse = supported(L, impl, case, n_splits)
+    reqs, heads = FULL[name]
+    if reqs is None:  # shortest, longest and one in between
+        order = np.argsort(case.lens)
+        reqs = sorted({int(order[0]), int(order[len(order) // 2]), int(order[-1])})
+    ro, rl = oracle_rows(case, reqs, heads)
+    o = out[reqs][:, :, heads]
+    l = lse[reqs][:, :, heads]
+    assert_parity(o, l, ro, rl, what=f"full {name}/{impl}")
+    assert not torch.isnan(out).any() and not torch.isnan(lse).any()
+
+
+def test_full_size_dcp_shards_and_merge(L, impl):
+    sc = synth.make_sharded_case(3, 32, 96, 142000, 8, device="cuda")
+    outs, lses = [], []
+    for sh in sc.shards:
+        o, l = supported(L, impl, sh, 0)
+        outs.append(o)
+        lses.append(l)
+    reqs, heads = [0, 31], [0, 50, 95]
+    ro, rl = oracle_rows(sc.shards[3], reqs, heads)
+    assert_parity(outs[3][reqs][:, :, heads], lses[3][reqs][:, :, heads], ro, rl, what="shard 3")
+    po, pl = torch.stack(outs), torch.stack(lses)
+    out = torch.full(po.shape[1:], float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full(pl.shape[1:], float("nan"), dtype=torch.float32, device="cuda")
+    L.mla_merge_partials(po, pl, 8, out, lse)
+    torch.cuda.synchronize()
+    ro, rl = oracle_rows(sc.full, reqs, heads)
+    assert_parity(out[reqs][:, :, heads], lse[reqs][:, :, heads], ro, rl, what="merged 142,000")
+    assert not torch.isnan(out).any()
