@@ -37,7 +37,7 @@ METRIC = "latent-KV GB/s (KV bytes read / decode-step time); decode steps/s; % o
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="tp8_batch")
@@ -69,31 +69,27 @@ def load_peaks():
     return 6800.0, "fallback (6.8 TB/s)"
 
 
-def kernel_source_sha():
-    h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "mla_latent_kv_fp8_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + fh.read())
-    return h.hexdigest()[:16]
+def source_sha(rel_path):
+    with open(os.path.join(ROOT, rel_path), "rb") as fh:
+        return hashlib.sha256(fh.read()).hexdigest()[:16]
 
 
 def ncu_traffic(kernel_family, workload):
-    """DRAM bytes per launch from a committed ncu summary, if its kernel source matches."""
+    """DRAM bytes per launch from a committed ncu summary, if the kernel's source file
+    is unchanged since the counters were taken (else null)."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
     e = d.get(f"{kernel_family}/{workload}")
-    if not e or e.get("source_sha") != kernel_source_sha():
+    if not e or e.get("source_sha") != source_sha(e["source_file"]):
         return None
     return e.get("dram_bytes_per_launch")
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms while running."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -107,7 +103,7 @@ class ClockSampler:
         try:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None

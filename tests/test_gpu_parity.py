@@ -185,7 +185,9 @@ def test_dcp_shards_merge_to_unsharded(L, impl):
 def test_merge_partials_matches_oracle(L, S, dtype):
     g = torch.Generator().manual_seed(S)
     rows = (3, 5)
-    po = torch.randn((S, *rows, 512), generator=g).to(dtype)
+    # attention outputs are weighted averages of latents: |o| well below 1 (at |o| >= 4
+    # bf16 rounding alone would exceed the 1e-2 absolute bound)
+    po = (0.25 * torch.randn((S, *rows, 512), generator=g)).to(dtype)
     pl = (torch.randn((S, *rows), generator=g) * 3).float()
     drop = torch.rand((S, *rows), generator=g) < 0.3
     pl[drop] = float("-inf")
