@@ -24,9 +24,14 @@
 //     two e4m3 terms p1 + p2 / 16 of 256 * P (relative error ~2^-8, the bf16
 //     level); the running output, max and normaliser live in registers of the
 //     correction warps and absorb each tile with exact fp32 LSE rescaling.
-//   * Warp roles: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps 4-7
-//     softmax (TMEM lanes of the score tile), warps 8-11 correction/epilogue
-//     (TMEM lanes = latent dims).  Every wait is bounded; on timeout the kernel
+//   * Warp roles: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer (a
+//     non-blocking event loop that runs QK^T up to four pages ahead of PV), and
+//     two attention warpgroups (warps 4-7 and 8-11) that take alternate pages.
+//     For its page a warpgroup reads the score tile (TMEM lane = position),
+//     computes the tile softmax, hands the quantised probabilities to the MMA
+//     issuer, and after PV folds the output tile (TMEM lane = latent dim) into
+//     its own running output, max and normaliser.  The two running states are
+//     merged once at the end.  Every wait is bounded; on timeout the kernel
 //     records an error, drains its own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -50,23 +55,29 @@ constexpr int kBoxBytes = kPage * 64;        // 4,096: 64 positions x 64 dims
 constexpr int kBoxes = kDqk / 64;            // 9
 constexpr int kQpBytes = kNqk * kDqk;        // 18,432
 constexpr int kPpBytes = kNqk * kPage;       // 2,048
+constexpr int kSBufs = 4;                    // score tiles in TMEM (QK^T look-ahead)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSCol0 = 0;               // S buffers: cols [0,32) and [32,64)
-constexpr uint32_t kOCol0 = 64;              // O buffers: cols [64,192) and [192,320)
+constexpr uint32_t kSCol0 = 0;               // S buffers: 4 x 64 cols at [0, 256): two
+                                             // accumulators (even / odd K-steps) of 32 cols
+constexpr uint32_t kSCols = 64;
+constexpr uint32_t kOCol0 = 256;             // O buffers: one per warpgroup, 2 x 128 cols
 constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per wait
 
 struct Smem {
     uint8_t slot[kStages][kSlotBytes];       // 1024-aligned page tiles
     uint8_t qp[kQpBytes];                    // [q1 | q2] K-major, no swizzle
-    uint8_t pp[2][kPpBytes];                 // [p1 | p2] K-major, no swizzle
-    float red_m[2][kNq][4];                  // per-warp tile maxima (softmax)
-    float red_l[2][kNq][4];                  // per-warp tile sums (-> correction)
-    float stat_m[2][kNq];                    // tile maxima (-> correction)
+    uint8_t pp[kSBufs][kPpBytes];            // [p1 | p2] K-major, no swizzle, per page
+    float red_m[2][2][kNq][4];               // [group][iter parity][head][warp] tile maxima
+    float red_l[2][2][kNq][4];               // [group][iter parity][head][warp] tile sums
+    float fin_m[kNq], fin_l[kNq];            // warpgroup 1's final max / normaliser
     float row_scale[kNq];                    // kv_scale * sm_scale * log2(e) * 2^-e
     int rowlim[kNq];                         // visible prefix per row; -1 = padding
     uint64_t full[kStages], empty[kStages];
-    uint64_t s_full[2], s_empty[2], p_full[2], o_full[2], o_empty[2], red_bar[2];
-    uint64_t mma_done;
+    uint64_t s_full[kSBufs], s_empty[kSBufs], p_full[kSBufs];
+    uint64_t o_full[2];                      // per warpgroup: its page's PV is complete
+    uint64_t red_bar[2][2];
+    uint64_t fin_bar;                        // warpgroup 1's final state is in shared memory
+    uint64_t mma_done[3];                    // per MMA-issuing thread: its MMAs drained
     uint32_t tmem_base;
     int abort;
 };
@@ -97,6 +108,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
     return ok != 0;
+}
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ float warp_max_redux(float v) {
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
 }
 __device__ __forceinline__ uint64_t global_ns() {
     uint64_t t;
@@ -189,6 +216,18 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
           "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
 }
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+          "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+          "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -227,6 +266,22 @@ __device__ __forceinline__ float warp_transpose_reduce(float (&v)[16], int lane)
     return kMax ? fmaxf(v[0], other) : v[0] + other;
 }
 
+// Two probabilities (times 256) -> e4m3 codes of p1 and of 16 * (value - p1),
+// computed in f16 (11 significant bits cover the 8 that p1 + p2/16 keeps).
+__device__ __forceinline__ void split_p(float a0, float a1, uint32_t& c1, uint32_t& c2) {
+    const __half2 h = __floats2half2_rn(a0, a1);
+    const __half2_raw hr = *reinterpret_cast<const __half2_raw*>(&h);
+    c1 = static_cast<uint32_t>(__nv_cvt_halfraw2_to_fp8x2(hr, __NV_SATFINITE, __NV_E4M3));
+    const __half2_raw br = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(c1), __NV_E4M3);
+    const __half2 back = *reinterpret_cast<const __half2*>(&br);
+    const __half2 r = __hmul2(__hsub2(h, back), __float2half2_rn(16.f));
+    c2 = static_cast<uint32_t>(
+        __nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&r), __NV_SATFINITE, __NV_E4M3));
+}
+
+// kRows: rows (t, h) this instantiation keeps in registers (12 or 16); the MMA
+// operands always use 16-row blocks (rows >= H*T are zero).
+template <int kRows>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_decode_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -253,15 +308,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&S.full[s], 1);
             mbar_init(&S.empty[s], 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kSBufs; ++i) {
             mbar_init(&S.s_full[i], 1);
             mbar_init(&S.s_empty[i], 4);
             mbar_init(&S.p_full[i], 4);
-            mbar_init(&S.o_full[i], 1);
-            mbar_init(&S.o_empty[i], 4);
-            mbar_init(&S.red_bar[i], 4);
         }
-        mbar_init(&S.mma_done, 1);
+        for (int g = 0; g < 2; ++g) {
+            mbar_init(&S.o_full[g], 1);
+            for (int i = 0; i < 2; ++i) mbar_init(&S.red_bar[g][i], 4);
+        }
+        mbar_init(&S.fin_bar, 4);
+        for (int i = 0; i < 3; ++i) mbar_init(&S.mma_done[i], 1);
         S.abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -289,8 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     amax = fmaxf(amax, fabsf(__uint_as_float(w[j] & 0xffff0000u)));
                 }
             }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            amax = warp_max_redux(amax);
             int e = 0;
             if (amax > 0.f && amax < INFINITY) e = max(-100, min(100, ilogbf(448.f / amax)));
             const float sc = ldexpf(1.f, e);
@@ -366,121 +422,137 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-    } else if (warp == 1) {
-        // ======================= MMA issuer =======================
+    } else if (warp == 1 || warp == 3) {
+        // ======================= QK^T issuers =======================
+        // Issuing one tcgen05.mma costs the issuing thread tens of cycles, so
+        // the MMAs are spread over three threads: warp 1 issues QK^T of the
+        // even pages, warp 3 of the odd pages, warp 2 all PV.  Each thread
+        // commits only to barriers that it alone signals.
         if (lane == 0 && n_pages > 0) {
-            const uint32_t qp = smem_u32(S.qp);
-            auto issue_qk = [&](int i) -> bool {
-                const int s = i % kStages, buf = i & 1;
-                if (!wait_bounded(&S.full[s], (i / kStages) & 1, abort, p.err)) return false;
-                if (!wait_bounded(&S.s_empty[buf], ((i >> 1) & 1) ^ 1, abort, p.err)) return false;
+            const uint64_t qd = smem_desc(smem_u32(S.qp), 128, (kDqk / 16) * 128, kLayoutNone);
+            for (int i = (warp == 1 ? 0 : 1); i < n_pages; i += 2) {
+                const int sb = i % kSBufs;
+                if (!wait_bounded(&S.full[i % kStages], (i / kStages) & 1, abort, p.err)) break;
+                if (!wait_bounded(&S.s_empty[sb], ((i / kSBufs) & 1) ^ 1, abort, p.err)) break;
                 tc_fence_after();
-                const uint32_t slot = smem_u32(S.slot[s]);
-                const uint32_t d = tmem + kSCol0 + 32 * buf;
+                const uint64_t ad = smem_desc(smem_u32(S.slot[i % kStages]), 16, 512, kLayoutSw64);
+                const uint32_t d = tmem + kSCol0 + kSCols * sb;
+                // Even and odd K-steps accumulate into two tiles (summed by the softmax).
 #pragma unroll
-                for (int ks = 0; ks < kDqk / 32; ++ks) {
-                    const uint64_t a = smem_desc(slot + (ks >> 1) * kBoxBytes + (ks & 1) * 32, 16, 512,
-                                                 kLayoutSw64);
-                    const uint64_t bd = smem_desc(qp + ks * 256, 128, (kDqk / 16) * 128, kLayoutNone);
-                    mma_e4m3(d, a, bd, kIdescQK, ks > 0);
-                }
-                mma_commit(&S.s_full[buf]);
-                return true;
-            };
-            bool ok = issue_qk(0);
-            for (int i = 0; ok && i < n_pages; ++i) {
-                if (i + 1 < n_pages && !(ok = issue_qk(i + 1))) break;
-                const int s = i % kStages, buf = i & 1;
-                if (!wait_bounded(&S.p_full[buf], (i >> 1) & 1, abort, p.err)) break;
-                if (!wait_bounded(&S.o_empty[buf], ((i >> 1) & 1) ^ 1, abort, p.err)) break;
-                tc_fence_after();
-                const uint32_t slot = smem_u32(S.slot[s]);
-                const uint32_t pp = smem_u32(S.pp[buf]);
-#pragma unroll
-                for (int c = 0; c < kDv / 128; ++c) {
-#pragma unroll
-                    for (int ks = 0; ks < kPage / 32; ++ks) {
-                        const uint64_t a = smem_desc(slot + 2 * c * kBoxBytes + ks * 32 * 64, kBoxBytes,
-                                                     512, kLayoutSw64);
-                        const uint64_t bd = smem_desc(pp + ks * 256, 128, (kPage / 16) * 128, kLayoutNone);
-                        mma_e4m3(tmem + kOCol0 + 128 * buf + 32 * c, a, bd, kIdescPV, ks > 0);
-                    }
-                }
-                mma_commit(&S.o_full[buf]);
-                mma_commit(&S.empty[s]);
+                for (int ks = 0; ks < kDqk / 32; ++ks)
+                    mma_e4m3(d + 32 * (ks & 1), ad + static_cast<uint64_t>(((ks >> 1) * kBoxBytes + (ks & 1) * 32) >> 4),
+                             qd + static_cast<uint64_t>(ks * 16), kIdescQK, ks > 1);
+                mma_commit(&S.s_full[sb]);
             }
-            // Drain: every MMA this thread issued completes before TMEM is freed.
-            mma_commit(&S.mma_done);
+            mma_commit(&S.mma_done[warp == 1 ? 0 : 1]);
             const uint64_t t0 = global_ns();
-            while (!mbar_try_wait(&S.mma_done, 0) && global_ns() - t0 < kTimeoutNs) {
+            while (!mbar_try_wait(&S.mma_done[warp == 1 ? 0 : 1], 0) && global_ns() - t0 < kTimeoutNs) {
             }
         }
-    } else if (warp >= 4 && warp < 8) {
-        // ======================= softmax =======================
+    } else if (warp == 2) {
+        // ======================= PV issuer =======================
+        // The output tile of warpgroup g is reused only after g has folded its
+        // previous page in, which g signals by its next p_full.
+        if (lane == 0 && n_pages > 0) {
+            for (int i = 0; i < n_pages; ++i) {
+                const int sb = i % kSBufs, g = i & 1, s = i % kStages;
+                if (!wait_bounded(&S.p_full[sb], (i / kSBufs) & 1, abort, p.err)) break;
+                tc_fence_after();
+                const uint64_t ad = smem_desc(smem_u32(S.slot[s]), kBoxBytes, 512, kLayoutSw64);
+                const uint64_t bd = smem_desc(smem_u32(S.pp[sb]), 128, (kPage / 16) * 128, kLayoutNone);
+                // K-step outer, 128-dim block inner: four independent accumulators.
+#pragma unroll
+                for (int ks = 0; ks < kPage / 32; ++ks)
+#pragma unroll
+                    for (int c = 0; c < kDv / 128; ++c)
+                        mma_e4m3(tmem + kOCol0 + 128 * g + 32 * c,
+                                 ad + static_cast<uint64_t>((2 * c * kBoxBytes + ks * 32 * 64) >> 4),
+                                 bd + static_cast<uint64_t>(ks * 16), kIdescPV, ks > 0);
+                mma_commit(&S.o_full[g]);
+                mma_commit(&S.empty[s]);
+            }
+            mma_commit(&S.mma_done[2]);
+            const uint64_t t0 = global_ns();
+            while (!mbar_try_wait(&S.mma_done[2], 0) && global_ns() - t0 < kTimeoutNs) {
+            }
+        }
+    } else if (warp >= 4) {
+        // ======================= attention warpgroups =======================
+        // Warpgroup g (warps 4-7: g = 0, warps 8-11: g = 1) owns pages i = g, g+2, ...
         // Every hand-off goes through an mbarrier with a bounded wait (no named
         // barriers), so a role that gives up can never leave another one blocked.
-        const int sw = warp - 4;                 // TMEM lane quadrant
+        const int g = (warp - 4) >> 2;
+        const int sw = warp & 3;                 // TMEM lane quadrant
         const bool has_row = lane < 16;          // M=64 score tile: 16 rows per quadrant
         const int pr = 16 * sw + lane;           // position within the page
+        const int d = 32 * sw + lane;            // latent dim within each 128-dim block
         const float NEG = -INFINITY;
-        for (int i = 0; i < n_pages; ++i) {
-            const int buf = i & 1;
-            if (!__all_sync(0xffffffffu, wait_bounded(&S.s_full[buf], (i >> 1) & 1, abort, p.err))) break;
+        float o[4][kRows];                       // running output, dims d + 128c
+        float m_run = NEG, l_run = 0.f;          // lane h < 16: head h
+#pragma unroll
+        for (int h = 0; h < kRows; ++h)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) o[c][h] = 0.f;
+        int k = 0;
+        for (int i = g; i < n_pages; i += 2, ++k) {
+            const int sb = i % kSBufs;           // score / probability buffer
+            const int kb = k & 1;                // this group's statistics buffer
+            // ---- scores of this page ----
+            if (!__all_sync(0xffffffffu, wait_bounded(&S.s_full[sb], (i / kSBufs) & 1, abort, p.err))) break;
             tc_fence_after();
-            uint32_t r1[16], r2[16];
-            const uint32_t ta = tmem + (static_cast<uint32_t>(32 * sw) << 16) + kSCol0 + 32 * buf;
-            tmem_ld16(ta, r1);
-            tmem_ld16(ta + 16, r2);
+            uint32_t r1[16], r2[16], r3[16], r4[16];
+            const uint32_t ta = tmem + (static_cast<uint32_t>(32 * sw) << 16) + kSCol0 + kSCols * sb;
+            tmem_ld16(ta, r1);       // even K-steps, q1 rows
+            tmem_ld16(ta + 16, r2);  // even K-steps, q2 rows
+            tmem_ld16(ta + 32, r3);  // odd K-steps, q1 rows
+            tmem_ld16(ta + 48, r4);  // odd K-steps, q2 rows
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&S.s_empty[buf]);
+            if (lane == 0) mbar_arrive(&S.s_empty[sb]);
 
             const int pg = pg_begin + i;
             const int32_t pid = __ldg(p.block_table + (int64_t)b * p.bt_stride + pg);
             const bool page_ok = pid >= 0 && pid < p.num_pages;
             const int pos = pg * kPage + pr;
             const bool in_part = has_row && page_ok && pos < p_end;
-            float s[kNq], e[kNq];
+            float s[kRows];
+            float mine = NEG;  // lane h < kRows ends up with this warp's max of head h
 #pragma unroll
-            for (int h = 0; h < kNq; ++h) {
-                const float v = (__uint_as_float(r1[h]) + __uint_as_float(r2[h]) * 0.0625f) * S.row_scale[h];
+            for (int h = 0; h < kRows; ++h) {
+                const float q1x = __uint_as_float(r1[h]) + __uint_as_float(r3[h]);
+                const float q2x = __uint_as_float(r2[h]) + __uint_as_float(r4[h]);
+                const float v = fmaf(q2x, 0.0625f, q1x) * S.row_scale[h];
                 s[h] = (in_part && pos < S.rowlim[h]) ? v : NEG;
+                const float wm = warp_max_redux(s[h]);
+                mine = (lane == h) ? wm : mine;
+            }
+            if (lane < kNq) S.red_m[g][kb][lane][sw] = mine;  // rows >= kRows: -inf
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.red_bar[g][kb]);
+            if (!__all_sync(0xffffffffu, wait_bounded(&S.red_bar[g][kb], (k >> 1) & 1, abort, p.err))) break;
+
+            // ---- tile softmax: P = 2^(s - m_tile) ----
+            float e[kNq];
+#pragma unroll
+            for (int h = 0; h < kNq; ++h) e[h] = 0.f;
+#pragma unroll
+            for (int h = 0; h < kRows; ++h) {
+                const float4 v = *reinterpret_cast<const float4*>(S.red_m[g][kb][h]);
+                const float m = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+                s[h] = (s[h] == NEG) ? 0.f : exp2f(s[h] - m);
                 e[h] = s[h];
             }
-            const float wmax = warp_transpose_reduce<true>(e, lane);
-            if ((lane & 1) == 0) S.red_m[buf][lane >> 1][sw] = wmax;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&S.red_bar[buf]);
-            if (!__all_sync(0xffffffffu, wait_bounded(&S.red_bar[buf], (i >> 1) & 1, abort, p.err))) break;
-            float m[kNq];
-#pragma unroll
-            for (int h = 0; h < kNq; ++h) {
-                const float4 v = *reinterpret_cast<const float4*>(S.red_m[buf][h]);
-                m[h] = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
-                e[h] = (s[h] == NEG) ? 0.f : exp2f(s[h] - m[h]);
-                s[h] = e[h];  // keep the probabilities; e is consumed by the sum
-            }
             const float wsum = warp_transpose_reduce<false>(e, lane);
-            // P and the statistics of buffer `buf` were last used by tile i - 2.
-            if (i >= 2 &&
-                !__all_sync(0xffffffffu, wait_bounded(&S.o_empty[buf], ((i >> 1) & 1) ^ 1, abort, p.err)))
-                break;
-            if ((lane & 1) == 0) {
-                S.red_l[buf][lane >> 1][sw] = wsum;
-                if (sw == 0) {
-                    const float4 v = *reinterpret_cast<const float4*>(S.red_m[buf][lane >> 1]);
-                    S.stat_m[buf][lane >> 1] = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
-                }
-            }
+            if ((lane & 1) == 0) S.red_l[g][kb][lane >> 1][sw] = wsum;
+            // Probability buffer sb was last read by PV(i - 4), which completed
+            // before this group's previous page's PV (already waited on).
             if (has_row) {
-                uint8_t* pp = S.pp[buf];
+                uint8_t* pp = S.pp[sb];
 #pragma unroll
                 for (int h = 0; h < kNq; h += 2) {
-                    const float a0 = s[h] * 256.f, a1 = s[h + 1] * 256.f;
-                    const uint32_t c1 = f2_to_e4m3x2(a0, a1);
-                    const float2 back = e4m3x2_to_f2(c1);
-                    const uint32_t c2 = f2_to_e4m3x2((a0 - back.x) * 16.f, (a1 - back.y) * 16.f);
+                    uint32_t c1 = 0, c2 = 0;
+                    if (h < kRows) split_p(s[h] * 256.f, s[h + 1] * 256.f, c1, c2);
                     pp[kmajor_off(h, pr, kPage)] = static_cast<uint8_t>(c1 & 0xff);
                     pp[kmajor_off(h + 1, pr, kPage)] = static_cast<uint8_t>(c1 >> 8);
                     pp[kmajor_off(kNq + h, pr, kPage)] = static_cast<uint8_t>(c2 & 0xff);
@@ -499,93 +571,108 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             fence_async_smem();
+            tc_fence_before();  // this group's previous TMEM output reads precede the next PV
             __syncwarp();
-            if (lane == 0) mbar_arrive(&S.p_full[buf]);
-        }
-    } else if (warp >= 8) {
-        // ======================= correction + epilogue =======================
-        // Thread (warp 8 + cw, lane) owns latent dims 32*cw + lane of each 128-dim
-        // block.  The running max / normaliser of head h is identical in every
-        // thread: lane h of each warp keeps it and broadcasts it by shuffle.
-        const int cw = warp - 8;
-        const int d = 32 * cw + lane;
-        float o[4][kNq];
-        float m_run = -INFINITY, l_run = 0.f;    // lane h < 16: head h
-#pragma unroll
-        for (int h = 0; h < kNq; ++h)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) o[c][h] = 0.f;
-        for (int i = 0; i < n_pages; ++i) {
-            const int buf = i & 1;
-            if (!__all_sync(0xffffffffu, wait_bounded(&S.o_full[buf], (i >> 1) & 1, abort, p.err))) break;
-            // p_full of this tile has completed (PV waited on it); waiting on it here
-            // orders the softmax's statistics writes before the reads below.
-            if (!__all_sync(0xffffffffu, wait_bounded(&S.p_full[buf], (i >> 1) & 1, abort, p.err))) break;
+            if (lane == 0) mbar_arrive(&S.p_full[sb]);
+
+            // ---- fold PV(i) into the running state ----
+            // Waiting on p_full (all four warps arrived) makes every warp's tile
+            // statistics visible; o_full[g] completes when PV(i) has.
+            if (!__all_sync(0xffffffffu, wait_bounded(&S.p_full[sb], (i / kSBufs) & 1, abort, p.err))) break;
+            if (!__all_sync(0xffffffffu, wait_bounded(&S.o_full[g], k & 1, abort, p.err))) break;
             tc_fence_after();
             float a_l = 1.f, b_l = 0.f;
-            if (lane < kNq) {
-                const float mt = S.stat_m[buf][lane];
-                const float4 lp = *reinterpret_cast<const float4*>(S.red_l[buf][lane]);
-                const float lt = (lp.x + lp.y) + (lp.z + lp.w);
+            if (lane < kRows) {
+                const float4 vm = *reinterpret_cast<const float4*>(S.red_m[g][kb][lane]);
+                const float4 vl = *reinterpret_cast<const float4*>(S.red_l[g][kb][lane]);
+                const float mt = fmaxf(fmaxf(vm.x, vm.y), fmaxf(vm.z, vm.w));
+                const float lt = (vl.x + vl.y) + (vl.z + vl.w);
                 const float mn = fmaxf(m_run, mt);
-                if (mn != -INFINITY) {
+                if (mn != NEG) {
                     a_l = exp2f(m_run - mn);
                     b_l = exp2f(mt - mn);
                     l_run = l_run * a_l + lt * b_l;
                     m_run = mn;
                 }
             }
-            float alpha[kNq], beta[kNq];
+            const uint32_t to = tmem + (static_cast<uint32_t>(32 * sw) << 16) + kOCol0 + 128 * g;
 #pragma unroll
-            for (int h = 0; h < kNq; ++h) {
-                alpha[h] = __shfl_sync(0xffffffffu, a_l, h);
-                beta[h] = __shfl_sync(0xffffffffu, b_l, h) * (1.f / 256.f);
-            }
-            const uint32_t ta = tmem + (static_cast<uint32_t>(32 * cw) << 16) + kOCol0 + 128 * buf;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t r[16];
-                tmem_ld16(ta + 32 * c, r);
+            for (int cc = 0; cc < 2; ++cc) {
+                uint32_t ra[32], rb[32];
+                tmem_ld32(to + 64 * cc, ra);
+                tmem_ld32(to + 64 * cc + 32, rb);
                 tmem_wait_ld();
 #pragma unroll
-                for (int h = 0; h < kNq; ++h) o[c][h] = fmaf(o[c][h], alpha[h], beta[h] * __uint_as_float(r[h]));
-                tmem_ld16(ta + 32 * c + 16, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int h = 0; h < kNq; ++h) o[c][h] = fmaf(beta[h] * 0.0625f, __uint_as_float(r[h]), o[c][h]);
+                for (int h = 0; h < kRows; ++h) {
+                    const float al = __shfl_sync(0xffffffffu, a_l, h);
+                    const float be = __shfl_sync(0xffffffffu, b_l, h) * (1.f / 256.f);
+                    const float va = fmaf(__uint_as_float(ra[16 + h]), 0.0625f, __uint_as_float(ra[h]));
+                    const float vb = fmaf(__uint_as_float(rb[16 + h]), 0.0625f, __uint_as_float(rb[h]));
+                    o[2 * cc][h] = fmaf(o[2 * cc][h], al, be * va);
+                    o[2 * cc + 1][h] = fmaf(o[2 * cc + 1][h], al, be * vb);
+                }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&S.o_empty[buf]);
         }
-        // epilogue: normalised partial answer (or final output) and its LSE
-        const bool direct = p.n_splits == 1;
+
+        // ---- merge the two warpgroups' running states; write the answer ----
+        // Warpgroup 1 parks its state in a page slot that no copy or MMA touches
+        // any more (the slot of its own last page, or an unused one).
+        const int j1 = (n_pages >= 2) ? ((n_pages % 2 == 0) ? n_pages - 1 : n_pages - 2) : -1;
+        float* park = reinterpret_cast<float*>(S.slot[j1 >= 0 ? j1 % kStages : kStages - 1]);
+        const int t_in_g = 32 * sw + lane;
+        if (g == 1) {
 #pragma unroll
-        for (int h = 0; h < kNq; ++h) {
-            const float l = __shfl_sync(0xffffffffu, l_run, h);
-            if (h >= HT) continue;
-            const int64_t grow = (int64_t)b * HT + h;
-            if (direct) {
-                const float inv = (l > 0.f) ? kv_scale / l : 0.f;
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int h = 0; h < kRows; ++h) park[(c * kRows + h) * 128 + t_in_g] = o[c][h];
+            if (sw == 0 && lane < kNq) {
+                S.fin_m[lane] = m_run;
+                S.fin_l[lane] = l_run;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.fin_bar);
+        } else {
+            const bool ok = __all_sync(0xffffffffu, wait_bounded(&S.fin_bar, 0, abort, p.err));
+            float a0 = 1.f, a1 = 0.f, l = l_run;
+            if (lane < kNq && ok) {
+                const float m1 = S.fin_m[lane], l1 = S.fin_l[lane];
+                const float mn = fmaxf(m_run, m1);
+                if (mn != NEG) {
+                    a0 = exp2f(m_run - mn);
+                    a1 = exp2f(m1 - mn);
+                    l = l_run * a0 + l1 * a1;
+                    m_run = mn;
+                }
+            }
+            const bool direct = p.n_splits == 1;
+#pragma unroll
+            for (int h = 0; h < kRows; ++h) {
+                const float c0 = __shfl_sync(0xffffffffu, a0, h);
+                const float c1 = __shfl_sync(0xffffffffu, a1, h);
+                const float lh = __shfl_sync(0xffffffffu, l, h);
+                if (h >= HT) continue;
+                const int64_t grow = (int64_t)b * HT + h;
+                const float inv = (lh > 0.f) ? kv_scale / lh : 0.f;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    __nv_bfloat16 v = __float2bfloat16_rn(o[c][h] * inv);
-                    p.out[grow * kDv + 128 * c + d] = *reinterpret_cast<uint16_t*>(&v);
+                    const float o1 = ok ? park[(c * kRows + h) * 128 + t_in_g] : 0.f;
+                    const float v = (o[c][h] * c0 + o1 * c1) * inv;
+                    if (direct) {
+                        __nv_bfloat16 bv = __float2bfloat16_rn(v);
+                        p.out[grow * kDv + 128 * c + d] = *reinterpret_cast<uint16_t*>(&bv);
+                    } else if (lh > 0.f) {
+                        p.part_out[((int64_t)split * p.B * HT + grow) * kDv + 128 * c + d] = v;
+                    }
                 }
-            } else if (l > 0.f) {
-                const float inv = kv_scale / l;
-                const int64_t prow = (int64_t)split * p.B * HT + grow;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) p.part_out[prow * kDv + 128 * c + d] = o[c][h] * inv;
             }
-        }
-        if (cw == 0 && lane < HT && lane < kNq) {
-            const float lse = (l_run > 0.f) ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
-            const int64_t grow = (int64_t)b * HT + lane;
-            if (direct) {
-                if (p.lse) p.lse[grow] = lse;
-            } else {
-                p.part_lse[(int64_t)split * p.B * HT + grow] = lse;
+            if (sw == 0 && lane < HT && lane < kNq) {
+                const float lse = (l > 0.f) ? (m_run + log2f(l)) * kLn2 : -INFINITY;
+                const int64_t grow = (int64_t)b * HT + lane;
+                if (direct) {
+                    if (p.lse) p.lse[grow] = lse;
+                } else {
+                    p.part_lse[(int64_t)split * p.B * HT + grow] = lse;
+                }
             }
         }
     }
@@ -655,7 +742,10 @@ cudaError_t launch_tc_decode(const DecodeParams& p, cudaStream_t stream, bool* h
                 return e;
             if ((e = cudaDeviceGetAttribute(&cc[dev][1], cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
                 return e;
-            if ((e = cudaFuncSetAttribute(tc_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if ((e = cudaFuncSetAttribute(tc_decode_kernel<12>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)sizeof(Smem) + 1024)) != cudaSuccess)
+                return e;
+            if ((e = cudaFuncSetAttribute(tc_decode_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           (int)sizeof(Smem) + 1024)) != cudaSuccess)
                 return e;
             cc_ready[dev] = true;
@@ -665,7 +755,10 @@ cudaError_t launch_tc_decode(const DecodeParams& p, cudaStream_t stream, bool* h
     CUtensorMap map;
     if ((e = encode_cache_map(&map, p.kv, p.num_pages)) != cudaSuccess) return e;
     dim3 grid(p.n_splits, p.B);
-    tc_decode_kernel<<<grid, kThreads, sizeof(Smem) + 1024, stream>>>(map, p);
+    if (p.H * p.T <= 12)
+        tc_decode_kernel<12><<<grid, kThreads, sizeof(Smem) + 1024, stream>>>(map, p);
+    else
+        tc_decode_kernel<16><<<grid, kThreads, sizeof(Smem) + 1024, stream>>>(map, p);
     e = cudaGetLastError();
     if (e == cudaSuccess) *handled = true;
     return e;
