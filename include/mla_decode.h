@@ -138,6 +138,32 @@ mla_status_t mla_merge_partials(const mla_tensor_t *partial_out, const mla_tenso
                                 int32_t n_shards, const mla_tensor_t *out,
                                 const mla_tensor_t *lse, void *stream);
 
+/*
+ * mla_decode_paged_noalloc -- the same operation as mla_decode_paged, with the
+ * same arguments and results, for callers that must not have the library
+ * allocate device memory: for example a serving engine that reserves nearly
+ * all of the GPU's memory for its own page pool and accounts for every byte,
+ * or a latency-critical decode step that must not pay for a first-use
+ * allocation.  (The post has no counterpart; this is a property of the
+ * library, not of the method.)
+ *
+ * The split partials live in one fixed device array of 8 MiB inside the
+ * library (every GPU that loads the library holds it until the process
+ * exits); this call never calls cudaMalloc, cudaMallocAsync or cudaFree.
+ * A call whose partials need more than 8 MiB (see
+ * mla_decode_workspace_bytes) returns MLA_ERR_UNSUPPORTED with a message and
+ * launches nothing; pass a smaller n_splits.  The first call on each device
+ * looks up the array's device address with that device current; make that
+ * first call before any stream capture.  All calls share the one array and
+ * it keeps the previous call's contents (nothing in it needs to start at
+ * zero): calls that overlap on the GPU, on any streams, race with each other.
+ */
+mla_status_t mla_decode_paged_noalloc(const mla_tensor_t *q, const mla_tensor_t *kv_cache,
+                                      const float *kv_scale, const mla_tensor_t *block_table,
+                                      const mla_tensor_t *seq_lens, int32_t n_splits,
+                                      float sm_scale, const mla_tensor_t *out,
+                                      const mla_tensor_t *lse, void *stream);
+
 /* The automatic split count used when n_splits == 0: enough history
  * partitions per request that B * splits fills every SM of the device
  * (at least one full wave), with at least 2 pages (128 positions) each.

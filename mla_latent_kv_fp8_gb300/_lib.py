@@ -26,7 +26,8 @@ _DTYPES = {torch.bfloat16: 1, torch.float32: 2, torch.uint8: 3, torch.float8_e4m
 # Every symbol include/mla_decode.h declares.
 EXPORTS = ("mla_decode_paged", "mla_merge_partials", "mla_auto_splits", "mla_split_chunk_pages",
            "mla_decode_workspace_bytes", "mla_set_impl", "mla_device_error", "mla_status_string",
-           "mla_last_error", "mla_profile_next_decode", "mla_last_decode_impl")
+           "mla_last_error", "mla_profile_next_decode", "mla_last_decode_impl",
+           "mla_decode_paged_noalloc")
 
 
 class MlaError(RuntimeError):
@@ -48,6 +49,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     P, T = ctypes.c_void_p, ctypes.POINTER(mla_tensor_t)
     lib.mla_decode_paged.argtypes = [T, T, P, T, T, ctypes.c_int32, ctypes.c_float, T, T, P]
     lib.mla_decode_paged.restype = ctypes.c_int
+    lib.mla_decode_paged_noalloc.argtypes = [T, T, P, T, T, ctypes.c_int32, ctypes.c_float, T, T, P]
+    lib.mla_decode_paged_noalloc.restype = ctypes.c_int
     lib.mla_merge_partials.argtypes = [T, T, ctypes.c_int32, T, T, P]
     lib.mla_merge_partials.restype = ctypes.c_int
     lib.mla_auto_splits.argtypes = [ctypes.c_int32] * 5
@@ -122,6 +125,16 @@ def mla_decode_paged(q, kv_cache, kv_scale, block_table, seq_lens, n_splits, sm_
     _check(lib().mla_decode_paged(_ref(dq), _ref(dkv), ctypes.c_void_p(kv_scale.data_ptr()),
                                   _ref(dbt), _ref(dsl), int(n_splits), float(sm_scale), _ref(do),
                                   _ref(dl), _stream(stream)))
+
+
+def mla_decode_paged_noalloc(q, kv_cache, kv_scale, block_table, seq_lens, n_splits, sm_scale, out,
+                             lse=None, stream=None):
+    """mla_decode_paged with its split scratch in the library's fixed 8 MiB device array."""
+    dq, dkv, dbt, dsl, do, dl = (describe(q), describe(kv_cache), describe(block_table),
+                                 describe(seq_lens), describe(out), describe(lse))
+    _check(lib().mla_decode_paged_noalloc(_ref(dq), _ref(dkv), ctypes.c_void_p(kv_scale.data_ptr()),
+                                          _ref(dbt), _ref(dsl), int(n_splits), float(sm_scale),
+                                          _ref(do), _ref(dl), _stream(stream)))
 
 
 def mla_merge_partials(partial_out, partial_lse, n_shards, out, lse=None, stream=None):

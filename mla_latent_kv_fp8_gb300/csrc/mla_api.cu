@@ -140,6 +140,25 @@ mla_status_t check_tensor(const mla_tensor_t* t, const char* name, int ndim, int
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 }  // namespace
+
+// Accessors for the library's other host translation units.
+mla_status_t internal_fail(mla_status_t st, const char* msg) { return fail(st, "%s", msg); }
+mla_status_t internal_cuda_fail(cudaError_t e, const char* what) { return cuda_fail(e, what); }
+void internal_clear_error() { t_last_error.clear(); }
+void internal_set_last_impl(int impl) { t_last_impl = impl; }
+mla_status_t internal_device(int** err_word, int* sm_count) {
+    DeviceInfo* d = nullptr;
+    mla_status_t st = device_info(&d);
+    if (st != MLA_OK) return st;
+    *err_word = d->err_word;
+    *sm_count = d->sm_count;
+    return MLA_OK;
+}
+mla_status_t internal_check_tensor(const mla_tensor_t* t, const char* name, int ndim, int dtype,
+                                   bool need_contig, size_t align) {
+    return check_tensor(t, name, ndim, dtype, need_contig, align);
+}
+
 }  // namespace mla
 
 using namespace mla;
