@@ -24,15 +24,17 @@
 //     two e4m3 terms p1 + p2 / 16 of 256 * P (relative error ~2^-8, the bf16
 //     level); the running output, max and normaliser live in registers of the
 //     correction warps and absorb each tile with exact fp32 LSE rescaling.
-//   * Warp roles: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer (a
-//     non-blocking event loop that runs QK^T up to four pages ahead of PV), and
-//     two attention warpgroups (warps 4-7 and 8-11) that take alternate pages.
-//     For its page a warpgroup reads the score tile (TMEM lane = position),
-//     computes the tile softmax, hands the quantised probabilities to the MMA
-//     issuer, and after PV folds the output tile (TMEM lane = latent dim) into
-//     its own running output, max and normaliser.  The two running states are
-//     merged once at the end.  Every wait is bounded; on timeout the kernel
-//     records an error, drains its own copies and MMAs, frees TMEM and returns.
+//   * Warp roles: warp 0 TMA producer; three MMA-issuing threads (warp 1: QK^T of
+//     even pages, warp 3: QK^T of odd pages, warp 2: PV of every page), because
+//     one thread can issue a tcgen05.mma only every ~50 cycles; and two
+//     attention warpgroups (warps 4-7, 8-11) that take alternate pages.  For its page a warpgroup reads the score tile (TMEM lane =
+//     position), computes the tile softmax, hands the quantised probabilities
+//     to the PV issuer and, after PV, folds the output tile (TMEM lane = latent
+//     dim) into its own running output; each thread also keeps fp32 partial
+//     normalisers of its positions, rescaled with the same factors.  The two
+//     running states are merged once at the end.
+//   * Every wait is bounded; on timeout the kernel records an error, drains its
+//     own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -46,7 +48,8 @@
 namespace mla {
 namespace {
 
-constexpr int kThreads = 384;
+constexpr int kGroups = 2;                   // attention warpgroups
+constexpr int kThreads = 128 + 128 * kGroups;
 constexpr int kStages = 5;                   // page slots in the TMA ring
 constexpr int kNq = 16;                      // rows (t, h) per CTA, padded
 constexpr int kNqk = 2 * kNq;                // MMA N: q1 rows | q2 rows (and p1 | p2)
@@ -57,26 +60,31 @@ constexpr int kQpBytes = kNqk * kDqk;        // 18,432
 constexpr int kPpBytes = kNqk * kPage;       // 2,048
 constexpr int kSBufs = 4;                    // score tiles in TMEM (QK^T look-ahead)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSCol0 = 0;               // S buffers: 4 x 64 cols at [0, 256): two
-                                             // accumulators (even / odd K-steps) of 32 cols
-constexpr uint32_t kSCols = 64;
-constexpr uint32_t kOCol0 = 256;             // O buffers: one per warpgroup, 2 x 128 cols
+constexpr uint32_t kSCol0 = 0;               // S buffers: 4 x 32 cols at [0, 128)
+constexpr uint32_t kSCols = 32;
+constexpr uint32_t kOCol0 = 128;             // O buffers: one per warpgroup, 128 cols each
 constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per wait
+constexpr float kHeadroom = 8.f;             // log2 units a score may exceed its head's reference
+constexpr float kShift = 4.f;                // a new reference sits this far below the page max
+static_assert(kOCol0 + 128 * kGroups <= kTmemCols, "TMEM budget");
+
 
 struct Smem {
     uint8_t slot[kStages][kSlotBytes];       // 1024-aligned page tiles
     uint8_t qp[kQpBytes];                    // [q1 | q2] K-major, no swizzle
-    uint8_t pp[kSBufs][kPpBytes];            // [p1 | p2] K-major, no swizzle, per page
-    float red_m[2][2][kNq][4];               // [group][iter parity][head][warp] tile maxima
-    float red_l[2][2][kNq][4];               // [group][iter parity][head][warp] tile sums
-    float fin_m[kNq], fin_l[kNq];            // warpgroup 1's final max / normaliser
+    uint8_t pp[kGroups][2][kPpBytes];        // [p1 | p2] MN-major, no swizzle, per group page
+    float red_m[kGroups][2][kNq][4];         // [group][iter parity][head][warp] tile maxima
+    float red_l[kGroups][kNq][4];            // per group: end-of-loop normaliser partials
+    float fin[kGroups][2][kNq];              // per group: final max / normaliser by head
     float row_scale[kNq];                    // kv_scale * sm_scale * log2(e) * 2^-e
     int rowlim[kNq];                         // visible prefix per row; -1 = padding
     uint64_t full[kStages], empty[kStages];
-    uint64_t s_full[kSBufs], s_empty[kSBufs], p_full[kSBufs];
-    uint64_t o_full[2];                      // per warpgroup: its page's PV is complete
-    uint64_t red_bar[2][2];
-    uint64_t fin_bar;                        // warpgroup 1's final state is in shared memory
+    uint64_t s_full[kSBufs], s_empty[kSBufs];
+    uint64_t p_full[kGroups][2];             // group's probabilities of its page are ready
+    uint64_t pv_done[kGroups][2];            // group's PV of its page k done (buffer k & 1)
+    uint64_t red_bar[kGroups][2];
+    uint64_t fin_l_bar[kGroups];             // group's normaliser partials are written
+    uint64_t fin_bar;                        // groups 1.. parked their final state
     uint64_t mma_done[3];                    // per MMA-issuing thread: its MMAs drained
     uint32_t tmem_base;
     int abort;
@@ -103,17 +111,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity)
@@ -147,6 +144,12 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, vol
             }
         }
     }
+}
+
+// Warp-wide bounded wait: every lane observes the phase flip itself (each lane
+// then holds its own acquire), and the warp agrees on the outcome.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* err) {
+    return __all_sync(0xffffffffu, wait_bounded(bar, parity, abort, err));
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
@@ -189,7 +192,7 @@ __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, bool a_mn_major,
            (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 constexpr uint32_t kIdescQK = idesc_e4m3(64, kNqk, false, false);
-constexpr uint32_t kIdescPV = idesc_e4m3(128, kNqk, true, false);
+constexpr uint32_t kIdescPV = idesc_e4m3(128, kNqk, true, true);
 
 __device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
                                          uint32_t accumulate) {
@@ -231,6 +234,37 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Barrier of the four warps of attention warpgroup g (named barrier 1 + g)
+// that also ORs a per-thread flag over them.  Shared-memory writes made before
+// it are visible to the group after it.
+__device__ __forceinline__ bool group_sync_or(int g, bool flag) {
+    uint32_t out;
+    __threadfence_block();
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.or.pred po, %2, 128, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(out)
+        : "r"(flag ? 1u : 0u), "r"(1 + g)
+        : "memory");
+    return out != 0;
+}
 
 // e4m3 helpers (round to nearest even, saturating to +-448)
 __device__ __forceinline__ uint32_t f2_to_e4m3x2(float a, float b) {
@@ -245,6 +279,17 @@ __device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t v) {
 // 8-row x 16-byte core matrices: LBO = 128 B along K, SBO = (K/16) * 128 along rows.
 __device__ __forceinline__ uint32_t kmajor_off(int n, int k, int K) {
     return (n & 7) * 16 + (n >> 3) * (K / 16) * 128 + (k & 15) + (k >> 4) * 128;
+}
+
+// Byte offset of (column n, position k) in the probability operand [p1 | p2]:
+// MN-major, no swizzle.  A core matrix is 8 positions x 16 columns (one
+// 16-byte row per position); the p1 and p2 core matrices of an 8-position
+// group sit side by side (128 B apart), and groups follow every 256 B.  One
+// position's 16 p1 codes are thus one 16-byte store, and so are its p2 codes.
+constexpr uint32_t kPpMnStride = 128;  // between the p1 and p2 core matrices
+constexpr uint32_t kPpKStride = 256;   // between 8-position groups
+__device__ __forceinline__ uint32_t pp_off(int n, int k) {
+    return (n >> 4) * kPpMnStride + (n & 15) + (k & 7) * 16 + (k >> 3) * kPpKStride;
 }
 
 // Transpose-reduce: 16 values per lane across the 32 lanes of a warp.  On
@@ -311,13 +356,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kSBufs; ++i) {
             mbar_init(&S.s_full[i], 1);
             mbar_init(&S.s_empty[i], 4);
-            mbar_init(&S.p_full[i], 4);
         }
-        for (int g = 0; g < 2; ++g) {
-            mbar_init(&S.o_full[g], 1);
-            for (int i = 0; i < 2; ++i) mbar_init(&S.red_bar[g][i], 4);
+        for (int g = 0; g < kGroups; ++g) {
+            mbar_init(&S.fin_l_bar[g], 4);
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(&S.pv_done[g][i], 1);
+                mbar_init(&S.p_full[g][i], 4);
+                mbar_init(&S.red_bar[g][i], 4);
+            }
         }
-        mbar_init(&S.fin_bar, 4);
+        mbar_init(&S.fin_bar, 4 * (kGroups - 1));
         for (int i = 0; i < 3; ++i) mbar_init(&S.mma_done[i], 1);
         S.abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -437,11 +485,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint64_t ad = smem_desc(smem_u32(S.slot[i % kStages]), 16, 512, kLayoutSw64);
                 const uint32_t d = tmem + kSCol0 + kSCols * sb;
-                // Even and odd K-steps accumulate into two tiles (summed by the softmax).
 #pragma unroll
                 for (int ks = 0; ks < kDqk / 32; ++ks)
-                    mma_e4m3(d + 32 * (ks & 1), ad + static_cast<uint64_t>(((ks >> 1) * kBoxBytes + (ks & 1) * 32) >> 4),
-                             qd + static_cast<uint64_t>(ks * 16), kIdescQK, ks > 1);
+                    mma_e4m3(d, ad + static_cast<uint64_t>(((ks >> 1) * kBoxBytes + (ks & 1) * 32) >> 4),
+                             qd + static_cast<uint64_t>(ks * 16), kIdescQK, ks > 0);
                 mma_commit(&S.s_full[sb]);
             }
             mma_commit(&S.mma_done[warp == 1 ? 0 : 1]);
@@ -451,15 +498,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 2) {
         // ======================= PV issuer =======================
-        // The output tile of warpgroup g is reused only after g has folded its
-        // previous page in, which g signals by its next p_full.
+        // Warpgroup g's output tile accumulates over all of g's pages.
         if (lane == 0 && n_pages > 0) {
             for (int i = 0; i < n_pages; ++i) {
-                const int sb = i % kSBufs, g = i & 1, s = i % kStages;
-                if (!wait_bounded(&S.p_full[sb], (i / kSBufs) & 1, abort, p.err)) break;
+                const int g = i % kGroups, k = i / kGroups, s = i % kStages;
+                if (!wait_bounded(&S.p_full[g][k & 1], (k >> 1) & 1, abort, p.err)) break;
                 tc_fence_after();
                 const uint64_t ad = smem_desc(smem_u32(S.slot[s]), kBoxBytes, 512, kLayoutSw64);
-                const uint64_t bd = smem_desc(smem_u32(S.pp[sb]), 128, (kPage / 16) * 128, kLayoutNone);
+                // MN-major, no swizzle: LBO = stride between 8-position groups (K),
+                // SBO = stride between the 16-column core matrices (N).
+                const uint64_t bd = smem_desc(smem_u32(S.pp[g][k & 1]), kPpKStride, kPpMnStride, kLayoutNone);
                 // K-step outer, 128-dim block inner: four independent accumulators.
 #pragma unroll
                 for (int ks = 0; ks < kPage / 32; ++ks)
@@ -467,8 +515,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < kDv / 128; ++c)
                         mma_e4m3(tmem + kOCol0 + 128 * g + 32 * c,
                                  ad + static_cast<uint64_t>((2 * c * kBoxBytes + ks * 32 * 64) >> 4),
-                                 bd + static_cast<uint64_t>(ks * 16), kIdescPV, ks > 0);
-                mma_commit(&S.o_full[g]);
+                                 bd + static_cast<uint64_t>((ks * 4 * kPpKStride) >> 4), kIdescPV,
+                                 k > 0 || ks > 0);
+                mma_commit(&S.pv_done[g][k & 1]);
                 mma_commit(&S.empty[s]);
             }
             mma_commit(&S.mma_done[2]);
@@ -478,185 +527,246 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= 4) {
         // ======================= attention warpgroups =======================
-        // Warpgroup g (warps 4-7: g = 0, warps 8-11: g = 1) owns pages i = g, g+2, ...
-        // Every hand-off goes through an mbarrier with a bounded wait (no named
-        // barriers), so a role that gives up can never leave another one blocked.
+        // Warpgroup g = (warp - 4) / 4 owns pages i = g, g + kGroups, ...  Its
+        // output tile accumulates in TMEM over all of those pages against a
+        // per-head reference r: the probabilities are P = 2^(s - r), and r moves
+        // only when a score would exceed r + kHeadroom, in which case the
+        // accumulated tile is rescaled in place.  The four warps of a group meet
+        // once per page at a named barrier that also ORs their failure flags, so
+        // they always leave the loop together; every other wait is a bounded
+        // mbarrier wait.
         const int g = (warp - 4) >> 2;
-        const int sw = warp & 3;                 // TMEM lane quadrant
+        const int quad = warp & 3;               // TMEM lane quadrant of this warp
         const bool has_row = lane < 16;          // M=64 score tile: 16 rows per quadrant
-        const int pr = 16 * sw + lane;           // position within the page
-        const int d = 32 * sw + lane;            // latent dim within each 128-dim block
+        const int pr = 16 * quad + lane;         // position within the page
+        const int d = 32 * quad + lane;          // latent dim within each 128-dim block
         const float NEG = -INFINITY;
-        float o[4][kRows];                       // running output, dims d + 128c
-        float m_run = NEG, l_run = 0.f;          // lane h < 16: head h
+        const bool causal = p.T > 1;             // for T = 1 the partition end bounds every row
+        const uint32_t to = tmem + (static_cast<uint32_t>(32 * quad) << 16) + kOCol0 + 128 * g;
+        const int32_t* bt = p.block_table + (int64_t)b * p.bt_stride + pg_begin;
+        float lp[kRows];                         // normaliser partials of this thread's positions
+        float r[kRows];                          // reference of each head (same in all lanes)
+        float rsc[kRows];                        // score scale of each row
+        float r_l = NEG;                         // lane h < kRows: r[h]
 #pragma unroll
-        for (int h = 0; h < kRows; ++h)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) o[c][h] = 0.f;
+        for (int h = 0; h < kRows; ++h) {
+            lp[h] = 0.f;
+            r[h] = NEG;
+            rsc[h] = S.row_scale[h];
+        }
+        bool fail = false;
         int k = 0;
-        for (int i = g; i < n_pages; i += 2, ++k) {
-            const int sb = i % kSBufs;           // score / probability buffer
-            const int kb = k & 1;                // this group's statistics buffer
-            // ---- scores of this page ----
-            if (!__all_sync(0xffffffffu, wait_bounded(&S.s_full[sb], (i / kSBufs) & 1, abort, p.err))) break;
-            tc_fence_after();
-            uint32_t r1[16], r2[16], r3[16], r4[16];
-            const uint32_t ta = tmem + (static_cast<uint32_t>(32 * sw) << 16) + kSCol0 + kSCols * sb;
-            tmem_ld16(ta, r1);       // even K-steps, q1 rows
-            tmem_ld16(ta + 16, r2);  // even K-steps, q2 rows
-            tmem_ld16(ta + 32, r3);  // odd K-steps, q1 rows
-            tmem_ld16(ta + 48, r4);  // odd K-steps, q2 rows
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&S.s_empty[sb]);
-
-            const int pg = pg_begin + i;
-            const int32_t pid = __ldg(p.block_table + (int64_t)b * p.bt_stride + pg);
+        int32_t pid_next = g < n_pages ? __ldg(bt + g) : 0;
+        for (int i = g; i < n_pages; i += kGroups, ++k) {
+            const int sb = i % kSBufs;           // score buffer
+            const int kb = k & 1;                // this group's probability / statistics buffer
+            const int32_t pid = pid_next;
+            if (i + kGroups < n_pages) pid_next = __ldg(bt + i + kGroups);
             const bool page_ok = pid >= 0 && pid < p.num_pages;
-            const int pos = pg * kPage + pr;
-            const bool in_part = has_row && page_ok && pos < p_end;
+            const int pos = (pg_begin + i) * kPage + pr;
             float s[kRows];
-            float mine = NEG;  // lane h < kRows ends up with this warp's max of head h
+            // ---- scores of this page; this warp's maximum of each head ----
+            if (!fail) fail = !warp_wait(&S.s_full[sb], (i / kSBufs) & 1, abort, p.err);
+            if (!fail) {
+                tc_fence_after();
+                uint32_t r1[16], r2[16];
+                const uint32_t ta = tmem + (static_cast<uint32_t>(32 * quad) << 16) + kSCol0 + kSCols * sb;
+                tmem_ld16(ta, r1);
+                tmem_ld16(ta + 16, r2);
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&S.s_empty[sb]);
+                const bool in_part = has_row && page_ok && pos < p_end;
+                float mine = NEG;  // lane h < kRows ends up with this warp's max of head h
 #pragma unroll
-            for (int h = 0; h < kRows; ++h) {
-                const float q1x = __uint_as_float(r1[h]) + __uint_as_float(r3[h]);
-                const float q2x = __uint_as_float(r2[h]) + __uint_as_float(r4[h]);
-                const float v = fmaf(q2x, 0.0625f, q1x) * S.row_scale[h];
-                s[h] = (in_part && pos < S.rowlim[h]) ? v : NEG;
-                const float wm = warp_max_redux(s[h]);
-                mine = (lane == h) ? wm : mine;
-            }
-            if (lane < kNq) S.red_m[g][kb][lane][sw] = mine;  // rows >= kRows: -inf
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&S.red_bar[g][kb]);
-            if (!__all_sync(0xffffffffu, wait_bounded(&S.red_bar[g][kb], (k >> 1) & 1, abort, p.err))) break;
-
-            // ---- tile softmax: P = 2^(s - m_tile) ----
-            float e[kNq];
-#pragma unroll
-            for (int h = 0; h < kNq; ++h) e[h] = 0.f;
-#pragma unroll
-            for (int h = 0; h < kRows; ++h) {
-                const float4 v = *reinterpret_cast<const float4*>(S.red_m[g][kb][h]);
-                const float m = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
-                s[h] = (s[h] == NEG) ? 0.f : exp2f(s[h] - m);
-                e[h] = s[h];
-            }
-            const float wsum = warp_transpose_reduce<false>(e, lane);
-            if ((lane & 1) == 0) S.red_l[g][kb][lane >> 1][sw] = wsum;
-            // Probability buffer sb was last read by PV(i - 4), which completed
-            // before this group's previous page's PV (already waited on).
-            if (has_row) {
-                uint8_t* pp = S.pp[sb];
-#pragma unroll
-                for (int h = 0; h < kNq; h += 2) {
-                    uint32_t c1 = 0, c2 = 0;
-                    if (h < kRows) split_p(s[h] * 256.f, s[h + 1] * 256.f, c1, c2);
-                    pp[kmajor_off(h, pr, kPage)] = static_cast<uint8_t>(c1 & 0xff);
-                    pp[kmajor_off(h + 1, pr, kPage)] = static_cast<uint8_t>(c1 >> 8);
-                    pp[kmajor_off(kNq + h, pr, kPage)] = static_cast<uint8_t>(c2 & 0xff);
-                    pp[kmajor_off(kNq + h + 1, pr, kPage)] = static_cast<uint8_t>(c2 >> 8);
+                for (int h = 0; h < kRows; ++h) {
+                    const float v = (__uint_as_float(r1[h]) + __uint_as_float(r2[h]) * 0.0625f) * rsc[h];
+                    s[h] = (in_part && (!causal || pos < S.rowlim[h])) ? v : NEG;
+                    const float wm = warp_max_redux(s[h]);
+                    mine = (lane == h) ? wm : mine;
                 }
-                // Rows past the partition's end (or of a page whose id was out of
-                // range) may hold anything, even NaN codes: zero them so that
-                // 0 * x stays 0 in the PV product.
-                if (!page_ok || pos >= p_end) {
-                    uint8_t* row = S.slot[i % kStages] + pr * 64;
+                if (lane < kNq) S.red_m[g][kb][lane][quad] = mine;  // rows >= kRows: -inf
+            }
+            if (group_sync_or(g, fail)) {
+                fail = true;
+                break;
+            }
+            // ---- page maxima; move the reference where a score would overflow ----
+            float t = NEG;
+            if (lane < kNq) {
+                const float4 vm = *reinterpret_cast<const float4*>(S.red_m[g][kb][lane]);
+                t = fmaxf(fmaxf(vm.x, vm.y), fmaxf(vm.z, vm.w));
+            }
+            const bool need = lane < kRows && t > r_l + kHeadroom;
+            if (__ballot_sync(0xffffffffu, need)) {
+                const float rn = need ? t - kShift : r_l;
+                const float a = need ? exp2f(r_l - rn) : 1.f;  // r_l = -inf: nothing to keep
+                r_l = rn;
+                float al[kRows];
 #pragma unroll
-                    for (int j = 0; j < kBoxes; ++j) {
-                        uint4* q4 = reinterpret_cast<uint4*>(row + j * kBoxBytes);
-                        q4[0] = q4[1] = q4[2] = q4[3] = make_uint4(0, 0, 0, 0);
+                for (int h = 0; h < kRows; ++h) {
+                    al[h] = __shfl_sync(0xffffffffu, a, h);
+                    r[h] = __shfl_sync(0xffffffffu, rn, h);
+                    lp[h] *= al[h];
+                }
+                if (k > 0) {
+                    // The tile holds PV of this group's pages 0..k-1: wait for the
+                    // last of them, then scale every head's columns.
+                    if (!warp_wait(&S.pv_done[g][(k - 1) & 1], ((k - 1) >> 1) & 1, abort, p.err)) {
+                        fail = true;
+                    } else {
+                        tc_fence_after();
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            uint32_t v[32];
+                            tmem_ld32(to + 32 * c, v);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                if ((j & 15) < kRows) v[j] = __float_as_uint(__uint_as_float(v[j]) * al[j & 15]);
+                            tmem_st32(to + 32 * c, v);
+                        }
+                        tmem_wait_st();
                     }
                 }
             }
-            fence_async_smem();
-            tc_fence_before();  // this group's previous TMEM output reads precede the next PV
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&S.p_full[sb]);
-
-            // ---- fold PV(i) into the running state ----
-            // Waiting on p_full (all four warps arrived) makes every warp's tile
-            // statistics visible; o_full[g] completes when PV(i) has.
-            if (!__all_sync(0xffffffffu, wait_bounded(&S.p_full[sb], (i / kSBufs) & 1, abort, p.err))) break;
-            if (!__all_sync(0xffffffffu, wait_bounded(&S.o_full[g], k & 1, abort, p.err))) break;
-            tc_fence_after();
-            float a_l = 1.f, b_l = 0.f;
-            if (lane < kRows) {
-                const float4 vm = *reinterpret_cast<const float4*>(S.red_m[g][kb][lane]);
-                const float4 vl = *reinterpret_cast<const float4*>(S.red_l[g][kb][lane]);
-                const float mt = fmaxf(fmaxf(vm.x, vm.y), fmaxf(vm.z, vm.w));
-                const float lt = (vl.x + vl.y) + (vl.z + vl.w);
-                const float mn = fmaxf(m_run, mt);
-                if (mn != NEG) {
-                    a_l = exp2f(m_run - mn);
-                    b_l = exp2f(mt - mn);
-                    l_run = l_run * a_l + lt * b_l;
-                    m_run = mn;
-                }
-            }
-            const uint32_t to = tmem + (static_cast<uint32_t>(32 * sw) << 16) + kOCol0 + 128 * g;
-#pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                uint32_t ra[32], rb[32];
-                tmem_ld32(to + 64 * cc, ra);
-                tmem_ld32(to + 64 * cc + 32, rb);
-                tmem_wait_ld();
+            // ---- probabilities of this page -> [p1 | p2] operand ----
+            // Buffer kb was last read by this group's PV two pages ago.
+            if (!fail && k >= 2) fail = !warp_wait(&S.pv_done[g][kb], ((k >> 1) - 1) & 1, abort, p.err);
+            if (!fail) {
 #pragma unroll
                 for (int h = 0; h < kRows; ++h) {
-                    const float al = __shfl_sync(0xffffffffu, a_l, h);
-                    const float be = __shfl_sync(0xffffffffu, b_l, h) * (1.f / 256.f);
-                    const float va = fmaf(__uint_as_float(ra[16 + h]), 0.0625f, __uint_as_float(ra[h]));
-                    const float vb = fmaf(__uint_as_float(rb[16 + h]), 0.0625f, __uint_as_float(rb[h]));
-                    o[2 * cc][h] = fmaf(o[2 * cc][h], al, be * va);
-                    o[2 * cc + 1][h] = fmaf(o[2 * cc + 1][h], al, be * vb);
+                    s[h] = (s[h] == NEG) ? 0.f : exp2f(s[h] - r[h]);
+                    lp[h] += s[h];
                 }
+                if (has_row) {
+                    uint32_t w1[4] = {0, 0, 0, 0}, w2[4] = {0, 0, 0, 0};
+#pragma unroll
+                    for (int h = 0; h < kRows; h += 2) {
+                        uint32_t c1, c2;
+                        split_p(s[h], s[h + 1], c1, c2);
+                        w1[h >> 2] |= (c1 & 0xffffu) << (8 * (h & 3));
+                        w2[h >> 2] |= (c2 & 0xffffu) << (8 * (h & 3));
+                    }
+                    uint8_t* pp = S.pp[g][kb];
+                    *reinterpret_cast<uint4*>(pp + pp_off(0, pr)) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+                    *reinterpret_cast<uint4*>(pp + pp_off(kNq, pr)) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
+                    // Rows past the partition's end (or of a page whose id was out of
+                    // range) may hold anything, even NaN codes: zero them so that
+                    // 0 * x stays 0 in the PV product.
+                    if (!page_ok || pos >= p_end) {
+                        uint8_t* row = S.slot[i % kStages] + pr * 64;
+#pragma unroll
+                        for (int j = 0; j < kBoxes; ++j) {
+                            uint4* q4 = reinterpret_cast<uint4*>(row + j * kBoxBytes);
+                            q4[0] = q4[1] = q4[2] = q4[3] = make_uint4(0, 0, 0, 0);
+                        }
+                    }
+                }
+                fence_async_smem();
+                tc_fence_before();  // TMEM stores of a rescale precede the next PV
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&S.p_full[g][kb]);
             }
         }
 
-        // ---- merge the two warpgroups' running states; write the answer ----
-        // Warpgroup 1 parks its state in a page slot that no copy or MMA touches
-        // any more (the slot of its own last page, or an unused one).
-        const int j1 = (n_pages >= 2) ? ((n_pages % 2 == 0) ? n_pages - 1 : n_pages - 2) : -1;
-        float* park = reinterpret_cast<float*>(S.slot[j1 >= 0 ? j1 % kStages : kStages - 1]);
-        const int t_in_g = 32 * sw + lane;
-        if (g == 1) {
+        // ---- the group's accumulated tile: O = D(p1) + D(p2) / 16 ----
+        const int cnt = n_pages > g ? (n_pages - g + kGroups - 1) / kGroups : 0;
+        bool o_ok = !fail && cnt > 0;
+        if (o_ok) o_ok = warp_wait(&S.pv_done[g][(cnt - 1) & 1], ((cnt - 1) >> 1) & 1, abort, p.err);
+        float o[4][kRows];
+        if (o_ok) tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint32_t v[32];
+            if (o_ok) {
+                tmem_ld32(to + 32 * c, v);
+                tmem_wait_ld();
+            }
+#pragma unroll
+            for (int h = 0; h < kRows; ++h)
+                o[c][h] = o_ok ? fmaf(__uint_as_float(v[16 + h]), 0.0625f, __uint_as_float(v[h])) : 0.f;
+        }
+        float m_run = r_l;
+
+        // ---- this group's normaliser: reduce the per-thread partials ----
+        {
+            float e[kNq];
+#pragma unroll
+            for (int h = 0; h < kNq; ++h) e[h] = h < kRows ? lp[h] : 0.f;
+            const float wsum = warp_transpose_reduce<false>(e, lane);
+            if ((lane & 1) == 0) S.red_l[g][lane >> 1][quad] = wsum;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.fin_l_bar[g]);
+        }
+        const bool l_ok = __all_sync(0xffffffffu, wait_bounded(&S.fin_l_bar[g], 0, abort, p.err));
+        float l_run = 0.f;  // lane h: normaliser of head h
+        if (lane < kNq && l_ok) {
+            const float4 vl = *reinterpret_cast<const float4*>(S.red_l[g][lane]);
+            l_run = (vl.x + vl.y) + (vl.z + vl.w);
+        }
+
+        // ---- merge the warpgroups' running states; write the answer ----
+        // Warpgroups 1.. park their state in a page slot that no copy or MMA
+        // touches any more: the slot of their own last page, or an unused one.
+        auto park_of = [&](int gg) -> float* {
+            const int c = n_pages > gg ? (n_pages - gg + kGroups - 1) / kGroups : 0;
+            const int sl = c > 0 ? (gg + kGroups * (c - 1)) % kStages : kStages - gg;
+            return reinterpret_cast<float*>(S.slot[sl]);
+        };
+        const int t_in_g = 32 * quad + lane;
+        if (g > 0) {
+            float* park = park_of(g);
 #pragma unroll
             for (int c = 0; c < 4; ++c)
 #pragma unroll
                 for (int h = 0; h < kRows; ++h) park[(c * kRows + h) * 128 + t_in_g] = o[c][h];
-            if (sw == 0 && lane < kNq) {
-                S.fin_m[lane] = m_run;
-                S.fin_l[lane] = l_run;
+            if (quad == 0 && lane < kNq) {
+                S.fin[g][0][lane] = m_run;
+                S.fin[g][1][lane] = l_run;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.fin_bar);
         } else {
             const bool ok = __all_sync(0xffffffffu, wait_bounded(&S.fin_bar, 0, abort, p.err));
-            float a0 = 1.f, a1 = 0.f, l = l_run;
+            // lane h: merged max, weights of the groups, merged normaliser
+            float wg[kGroups], l = l_run;
+            wg[0] = 1.f;
+#pragma unroll
+            for (int gg = 1; gg < kGroups; ++gg) wg[gg] = 0.f;
             if (lane < kNq && ok) {
-                const float m1 = S.fin_m[lane], l1 = S.fin_l[lane];
-                const float mn = fmaxf(m_run, m1);
+                float mn = m_run;
+#pragma unroll
+                for (int gg = 1; gg < kGroups; ++gg) mn = fmaxf(mn, S.fin[gg][0][lane]);
                 if (mn != NEG) {
-                    a0 = exp2f(m_run - mn);
-                    a1 = exp2f(m1 - mn);
-                    l = l_run * a0 + l1 * a1;
+                    wg[0] = exp2f(m_run - mn);
+                    l = l_run * wg[0];
+#pragma unroll
+                    for (int gg = 1; gg < kGroups; ++gg) {
+                        wg[gg] = exp2f(S.fin[gg][0][lane] - mn);
+                        l += S.fin[gg][1][lane] * wg[gg];
+                    }
                     m_run = mn;
                 }
             }
             const bool direct = p.n_splits == 1;
 #pragma unroll
             for (int h = 0; h < kRows; ++h) {
-                const float c0 = __shfl_sync(0xffffffffu, a0, h);
-                const float c1 = __shfl_sync(0xffffffffu, a1, h);
+                float w[kGroups];
+#pragma unroll
+                for (int gg = 0; gg < kGroups; ++gg) w[gg] = __shfl_sync(0xffffffffu, wg[gg], h);
                 const float lh = __shfl_sync(0xffffffffu, l, h);
                 if (h >= HT) continue;
                 const int64_t grow = (int64_t)b * HT + h;
                 const float inv = (lh > 0.f) ? kv_scale / lh : 0.f;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    const float o1 = ok ? park[(c * kRows + h) * 128 + t_in_g] : 0.f;
-                    const float v = (o[c][h] * c0 + o1 * c1) * inv;
+                    float v = o[c][h] * w[0];
+#pragma unroll
+                    for (int gg = 1; gg < kGroups; ++gg)
+                        if (ok) v = fmaf(park_of(gg)[(c * kRows + h) * 128 + t_in_g], w[gg], v);
+                    v *= inv;
                     if (direct) {
                         __nv_bfloat16 bv = __float2bfloat16_rn(v);
                         p.out[grow * kDv + 128 * c + d] = *reinterpret_cast<uint16_t*>(&bv);
@@ -665,7 +775,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (sw == 0 && lane < HT && lane < kNq) {
+            if (quad == 0 && lane < HT && lane < kNq) {
                 const float lse = (l > 0.f) ? (m_run + log2f(l)) * kLn2 : -INFINITY;
                 const int64_t grow = (int64_t)b * HT + lane;
                 if (direct) {
@@ -752,6 +862,7 @@ cudaError_t launch_tc_decode(const DecodeParams& p, cudaStream_t stream, bool* h
         }
     }
     if (!tc_supports(p, cc[dev][0], cc[dev][1])) return cudaSuccess;
+
     CUtensorMap map;
     if ((e = encode_cache_map(&map, p.kv, p.num_pages)) != cudaSuccess) return e;
     dim3 grid(p.n_splits, p.B);

@@ -103,7 +103,7 @@ def test_reduced_workloads_match_oracle(L, impl, name, n_splits):
 @pytest.mark.parametrize("lens,H,T", [
     ([1], 12, 1), ([64], 12, 1), ([65], 12, 1), ([128, 129, 127], 12, 1), ([4, 5, 68], 12, 4),
     ([0, 300, 0], 12, 1), ([200], 1, 1), ([333, 17], 7, 3), ([260], 128, 1), ([190, 66], 32, 4),
-    ([517], 16, 8), ([1000], 96, 1)])
+    ([517], 16, 8), ([1000], 96, 1), ([300, 77], 14, 1), ([260, 9], 4, 4), ([700], 16, 1)])
 def test_edge_shapes_match_oracle(L, impl, lens, H, T):
     case = synth.make_decode_case(1000 + sum(lens) + H + T, lens, H, T, extra_pages=3)
     for n_splits in (0, 1, 3):
