@@ -249,6 +249,17 @@ __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// True in exactly one lane of a converged warp.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b32 r;\n\t"
+        "elect.sync r|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // Barrier of the four warps of attention warpgroup g (named barrier 1 + g)
 // that also ORs a per-thread flag over them.  Shared-memory writes made before
 // it are visible to the group after it.
@@ -476,54 +487,77 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the MMAs are spread over three threads: warp 1 issues QK^T of the
         // even pages, warp 3 of the odd pages, warp 2 all PV.  Each thread
         // commits only to barriers that it alone signals.
-        if (lane == 0 && n_pages > 0) {
+        // The whole warp runs the loop (descriptors stay warp-uniform); one
+        // elected lane issues the MMAs and their commit.
+        if (n_pages > 0) {
+            const bool leader = elect_one();
             const uint64_t qd = smem_desc(smem_u32(S.qp), 128, (kDqk / 16) * 128, kLayoutNone);
             for (int i = (warp == 1 ? 0 : 1); i < n_pages; i += 2) {
                 const int sb = i % kSBufs;
-                if (!wait_bounded(&S.full[i % kStages], (i / kStages) & 1, abort, p.err)) break;
-                if (!wait_bounded(&S.s_empty[sb], ((i / kSBufs) & 1) ^ 1, abort, p.err)) break;
+                // With an odd ring, slot i % kStages last held page i - kStages of
+                // the other issuer.  A parity test of full[] is exact only if that
+                // page's phase has completed, so first wait for its PV (which also
+                // gates the copy of page i): without it a parity two phases behind
+                // would read as complete.
+                if (i >= kStages && !warp_wait(&S.empty[i % kStages], ((i / kStages) & 1) ^ 1, abort, p.err))
+                    break;
+                if (!warp_wait(&S.full[i % kStages], (i / kStages) & 1, abort, p.err)) break;
+                if (!warp_wait(&S.s_empty[sb], ((i / kSBufs) & 1) ^ 1, abort, p.err)) break;
                 tc_fence_after();
                 const uint64_t ad = smem_desc(smem_u32(S.slot[i % kStages]), 16, 512, kLayoutSw64);
                 const uint32_t d = tmem + kSCol0 + kSCols * sb;
+                if (leader) {
 #pragma unroll
-                for (int ks = 0; ks < kDqk / 32; ++ks)
-                    mma_e4m3(d, ad + static_cast<uint64_t>(((ks >> 1) * kBoxBytes + (ks & 1) * 32) >> 4),
-                             qd + static_cast<uint64_t>(ks * 16), kIdescQK, ks > 0);
-                mma_commit(&S.s_full[sb]);
+                    for (int ks = 0; ks < kDqk / 32; ++ks)
+                        mma_e4m3(d, ad + static_cast<uint64_t>(((ks >> 1) * kBoxBytes + (ks & 1) * 32) >> 4),
+                                 qd + static_cast<uint64_t>(ks * 16), kIdescQK, ks > 0);
+                    mma_commit(&S.s_full[sb]);
+                }
+                __syncwarp();
             }
-            mma_commit(&S.mma_done[warp == 1 ? 0 : 1]);
-            const uint64_t t0 = global_ns();
-            while (!mbar_try_wait(&S.mma_done[warp == 1 ? 0 : 1], 0) && global_ns() - t0 < kTimeoutNs) {
+            if (leader) {
+                mma_commit(&S.mma_done[warp == 1 ? 0 : 1]);
+                const uint64_t t0 = global_ns();
+                while (!mbar_try_wait(&S.mma_done[warp == 1 ? 0 : 1], 0) && global_ns() - t0 < kTimeoutNs) {
+                }
             }
+            __syncwarp();
         }
     } else if (warp == 2) {
         // ======================= PV issuer =======================
         // Warpgroup g's output tile accumulates over all of g's pages.
-        if (lane == 0 && n_pages > 0) {
+        if (n_pages > 0) {
+            const bool leader = elect_one();
             for (int i = 0; i < n_pages; ++i) {
                 const int g = i % kGroups, k = i / kGroups, s = i % kStages;
-                if (!wait_bounded(&S.p_full[g][k & 1], (k >> 1) & 1, abort, p.err)) break;
+                if (!warp_wait(&S.p_full[g][k & 1], (k >> 1) & 1, abort, p.err)) break;
                 tc_fence_after();
                 const uint64_t ad = smem_desc(smem_u32(S.slot[s]), kBoxBytes, 512, kLayoutSw64);
                 // MN-major, no swizzle: LBO = stride between 8-position groups (K),
                 // SBO = stride between the 16-column core matrices (N).
                 const uint64_t bd = smem_desc(smem_u32(S.pp[g][k & 1]), kPpKStride, kPpMnStride, kLayoutNone);
                 // K-step outer, 128-dim block inner: four independent accumulators.
+                if (leader) {
 #pragma unroll
-                for (int ks = 0; ks < kPage / 32; ++ks)
+                    for (int ks = 0; ks < kPage / 32; ++ks)
 #pragma unroll
-                    for (int c = 0; c < kDv / 128; ++c)
-                        mma_e4m3(tmem + kOCol0 + 128 * g + 32 * c,
-                                 ad + static_cast<uint64_t>((2 * c * kBoxBytes + ks * 32 * 64) >> 4),
-                                 bd + static_cast<uint64_t>((ks * 4 * kPpKStride) >> 4), kIdescPV,
-                                 k > 0 || ks > 0);
-                mma_commit(&S.pv_done[g][k & 1]);
-                mma_commit(&S.empty[s]);
+                        for (int c = 0; c < kDv / 128; ++c)
+                            mma_e4m3(tmem + kOCol0 + 128 * g + 32 * c,
+                                     ad + static_cast<uint64_t>((2 * c * kBoxBytes + ks * 32 * 64) >> 4),
+                                     bd + static_cast<uint64_t>((ks * 4 * kPpKStride) >> 4), kIdescPV,
+                                     k > 0 || ks > 0);
+                    mma_commit(&S.pv_done[g][k & 1]);
+                    mma_commit(&S.empty[s]);
+                }
+                __syncwarp();
             }
-            mma_commit(&S.mma_done[2]);
-            const uint64_t t0 = global_ns();
-            while (!mbar_try_wait(&S.mma_done[2], 0) && global_ns() - t0 < kTimeoutNs) {
+            if (leader) {
+                mma_commit(&S.mma_done[2]);
+                const uint64_t t0 = global_ns();
+                while (!mbar_try_wait(&S.mma_done[2], 0) && global_ns() - t0 < kTimeoutNs) {
+                }
             }
+            __syncwarp();
         }
     } else if (warp >= 4) {
         // ======================= attention warpgroups =======================
