@@ -78,15 +78,26 @@ __global__ void __launch_bounds__(256) merge_warp_kernel(MergeParams p) {
     const float e = (ls == -INFINITY) ? 0.f : exp2f((ls - M) * kLog2e);
     const float sum = warp_sum(e);
     const float w = e / sum;
+    // Eight parts per round: all eight loads are in flight before the first
+    // product, so a round costs one memory latency, not eight.
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < p.S; ++s) {
-        const float ws = __shfl_sync(0xffffffffu, w, s);
-        if (ws == 0.f) continue;
-        const float4 v = load4<kBf16In>(p.part_out, ((int64_t)s * p.rows + row) * kDv + col);
-        acc.x = fmaf(ws, v.x, acc.x);
-        acc.y = fmaf(ws, v.y, acc.y);
-        acc.z = fmaf(ws, v.z, acc.z);
-        acc.w = fmaf(ws, v.w, acc.w);
+    for (int s0 = 0; s0 < p.S; s0 += 8) {
+        float ws[8];
+        float4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            ws[j] = __shfl_sync(0xffffffffu, w, (s0 + j) & 31);
+            if (s0 + j >= p.S) ws[j] = 0.f;
+            v[j] = ws[j] != 0.f ? load4<kBf16In>(p.part_out, ((int64_t)(s0 + j) * p.rows + row) * kDv + col)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            acc.x = fmaf(ws[j], v[j].x, acc.x);
+            acc.y = fmaf(ws[j], v[j].y, acc.y);
+            acc.z = fmaf(ws[j], v[j].z, acc.z);
+            acc.w = fmaf(ws[j], v[j].w, acc.w);
+        }
     }
     __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
     __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
@@ -133,13 +144,21 @@ __global__ void __launch_bounds__(256) merge_cta_kernel(MergeParams p) {
     for (int i = 0; i < 8; ++i) sum += red[i];
     const float lse_out = M + logf(sum);
 
+    // Warp wid takes parts wid, wid + 8, ...; eight of them per round, with
+    // every load of the round issued before the first product.  An empty
+    // part's output was never written: it is selected away, not multiplied.
     float acc = 0.f;
-#pragma unroll 4
-    for (int s = wid; s < p.S; s += 8) {
-        const float ls = p.part_lse[(int64_t)s * p.rows + row];
-        if (ls == -INFINITY) continue;
-        const float w = exp2f((ls - lse_out) * kLog2e);
-        acc = fmaf(w, load1<kBf16In>(p.part_out, ((int64_t)s * p.rows + row) * kDv + col), acc);
+    for (int s0 = wid; s0 < p.S; s0 += 64) {
+        float ls[8], v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int s = s0 + 8 * j;
+            ls[j] = s < p.S ? p.part_lse[(int64_t)s * p.rows + row] : -INFINITY;
+            v[j] = s < p.S ? load1<kBf16In>(p.part_out, ((int64_t)s * p.rows + row) * kDv + col) : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (ls[j] != -INFINITY) acc = fmaf(exp2f((ls[j] - lse_out) * kLog2e), v[j], acc);
     }
     part[wid][lane] = acc;
     __syncthreads();

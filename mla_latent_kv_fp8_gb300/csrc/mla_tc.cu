@@ -347,16 +347,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int HT = p.H * p.T;
     volatile int* abort = &S.abort;
 
+    // Global loads that depend only on the launch indices go out together,
+    // before any of their values is needed: the producer's first 64 page ids
+    // (one per lane, in two windows of 32) and the query rows of warps 1..11.
+    const int pg_begin = split * p.chunk_pages;
+    const int32_t* bt_cta = p.block_table + (int64_t)b * p.bt_stride + pg_begin;
+    int32_t pid_cur = 0, pid_nxt = 0;
+    uint4 qv[2][3];  // rows warp - 1 and warp + 10, 16-byte chunks lane + 32k
+    if (warp == 0) {
+        if (lane == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
+        pid_cur = pg_begin + lane < p.max_pages ? __ldg(bt_cta + lane) : 0;
+        pid_nxt = pg_begin + 32 + lane < p.max_pages ? __ldg(bt_cta + 32 + lane) : 0;
+    } else {
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            const int r = warp - 1 + (kThreads / 32 - 1) * rr;
+            const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)b * HT + r) * kDqk);
+#pragma unroll
+            for (int k = 0; k < 3; ++k) {
+                const int c = lane + 32 * k;  // 16-byte chunk: 8 bf16 values
+                qv[rr][k] = (r < kNq && r < HT && c < kDqk / 8) ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+            }
+        }
+    }
     int L = __ldg(p.seq_lens + b);
+    const float kv_scale = __ldg(p.kv_scale);
     if (L < 0 || L > p.max_pages * kPage || (L > 0 && L < p.T)) {
         if (tid == 0) atomicCAS(p.err, 0, kErrSeqRange);
         L = 0;
     }
-    const int p_begin = split * p.chunk_pages * kPage;
+    const int p_begin = pg_begin * kPage;
     const int p_end = min(L, p_begin + p.chunk_pages * kPage);
-    const int pg_begin = p_begin / kPage;
     const int n_pages = p_end > p_begin ? (p_end - p_begin + kPage - 1) / kPage : 0;
-    const float kv_scale = __ldg(p.kv_scale);
 
     // ---------------- set-up: barriers, TMEM, query operand ----------------
     if (tid == 0) {
@@ -380,6 +402,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 3; ++i) mbar_init(&S.mma_done[i], 1);
         S.abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncthreads();  // barriers initialised
+    // The producer (warp 0) starts the first copies at once and takes no part in
+    // the rest of the set-up: issuing a copy can stall its thread for a long
+    // time, and the other warps prepare the query and TMEM meanwhile.
+    int issued = 0;
+    auto issue_page = [&](int i, int32_t pid) {  // one thread
+        const int s = i % kStages;
+        if (pid < 0 || pid >= p.num_pages) {
+            atomicCAS(p.err, 0, kErrPageRange);
+            pid = 0;  // load a valid page; the softmax masks and zeroes it
+        }
+        mbar_expect_tx(&S.full[s], kSlotBytes);
+        const uint32_t dst = smem_u32(S.slot[s]);
+#pragma unroll
+        for (int j = 0; j < kBoxes; ++j) tma_load_2d(dst + j * kBoxBytes, &tmap, 64 * j, pid * kPage, &S.full[s]);
+    };
+    if (warp == 0 && n_pages > 0) {
+        const int first = min(kStages, n_pages);  // fresh slots: nothing to wait for
+        for (int i = 0; i < first; ++i) {
+            const int32_t pid = __shfl_sync(0xffffffffu, pid_cur, i);
+            if (lane == 0) issue_page(i, pid);
+        }
+        issued = first;
+        __syncwarp();
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -388,16 +436,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    // Query rows: warp w prepares rows w and w + 12 (< 16).
-    for (int r = warp; r < kNq; r += kThreads / 32) {
+    // Query rows: warps 1..11 prepare rows warp - 1 and warp + 10 (< 16).
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+        const int r = warp - 1 + (kThreads / 32 - 1) * rr;
+        if (warp == 0 || r >= kNq) continue;
         if (r < HT) {
-            const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)b * HT + r) * kDqk);
-            uint4 v[3];
+            const uint4* v = qv[rr];
             float amax = 0.f;
 #pragma unroll
             for (int k = 0; k < 3; ++k) {
-                const int c = lane + 32 * k;  // 16-byte chunk: 8 bf16 values
-                v[k] = c < kDqk / 8 ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
                 const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -446,31 +494,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     fence_async_smem();  // query operand: generic writes -> tensor-core reads
     tc_fence_before();
-    __syncthreads();
+    if (warp > 0) asm volatile("bar.sync 3, %0;" ::"n"(kThreads - 32) : "memory");  // warps 1..11
     tc_fence_after();
-    const uint32_t tmem = S.tmem_base;
+    const uint32_t tmem = warp > 0 ? S.tmem_base : 0u;
     asm volatile("griddepcontrol.launch_dependents;");
 
     if (warp == 0) {
         // ======================= TMA producer =======================
-        if (lane == 0 && n_pages > 0) {
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
-            int issued = 0;
-            for (int i = 0; i < n_pages; ++i) {
-                const int s = i % kStages;
-                if (!wait_bounded(&S.empty[s], ((i / kStages) & 1) ^ 1, abort, p.err)) break;
-                int32_t pid = __ldg(p.block_table + (int64_t)b * p.bt_stride + pg_begin + i);
-                if (pid < 0 || pid >= p.num_pages) {
-                    atomicCAS(p.err, 0, kErrPageRange);
-                    pid = 0;  // load a valid page; the softmax masks and zeroes it
+        if (n_pages > 0) {
+            for (int i = issued; i < n_pages; ++i) {
+                if ((i & 31) == 0) {  // next window of page ids; prefetch the one after
+                    pid_cur = pid_nxt;
+                    pid_nxt = i + 32 + lane < n_pages ? __ldg(bt_cta + i + 32 + lane) : 0;
                 }
-                mbar_expect_tx(&S.full[s], kSlotBytes);
-                const uint32_t dst = smem_u32(S.slot[s]);
-#pragma unroll
-                for (int j = 0; j < kBoxes; ++j)
-                    tma_load_2d(dst + j * kBoxBytes, &tmap, 64 * j, pid * kPage, &S.full[s]);
+                const int32_t pid = __shfl_sync(0xffffffffu, pid_cur, i & 31);
+                if (!warp_wait(&S.empty[i % kStages], ((i / kStages) & 1) ^ 1, abort, p.err)) break;
+                if (lane == 0) issue_page(i, pid);
+                __syncwarp();
                 issued = i + 1;
             }
+        }
+        if (lane == 0 && n_pages > 0) {
             // Drain: never leave with a copy in flight into this CTA's shared memory.
             for (int i = max(0, issued - kStages); i < issued; ++i) {
                 const int s = i % kStages;
