@@ -9,9 +9,9 @@
 // Parts with lse_s = -inf weigh exactly 0 and are not read.
 //
 // Two kernels:
-//   * few parts (S <= 32): one warp per (row, 128 value dims); lane s holds
-//     lse_s, the normaliser is a shuffle reduction, each lane streams 4 dims
-//     of every part with one vector load per part;
+//   * few parts (S <= 32): one warp per (row, 64 value dims); lane s holds
+//     lse_s, the normaliser is a shuffle reduction, each lane loads 2 dims of
+//     every part, all parts in one round;
 //   * many parts (S > 32, the in-GPU split combine of one long request): one
 //     CTA per (row, 32 value dims); the eight warps split the parts, each lane
 //     owns one dim, and the warps' sums meet in shared memory.
@@ -38,17 +38,6 @@ __device__ __forceinline__ void wait_for_producer(int pdl) {
 }
 
 template <bool kBf16In>
-__device__ __forceinline__ float4 load4(const void* base, int64_t idx) {
-    if constexpr (kBf16In) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + idx);
-        return make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xffff0000u),
-                           __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xffff0000u));
-    } else {
-        return *reinterpret_cast<const float4*>(static_cast<const float*>(base) + idx);
-    }
-}
-
-template <bool kBf16In>
 __device__ __forceinline__ float load1(const void* base, int64_t idx) {
     if constexpr (kBf16In) {
         return __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t*>(base)[idx]) << 16);
@@ -58,51 +47,56 @@ __device__ __forceinline__ float load1(const void* base, int64_t idx) {
 }
 
 template <bool kBf16In>
+__device__ __forceinline__ float2 load2(const void* base, int64_t idx) {
+    if constexpr (kBf16In) {
+        const uint32_t raw = *reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(base) + idx);
+        return make_float2(__uint_as_float(raw << 16), __uint_as_float(raw & 0xffff0000u));
+    } else {
+        return *reinterpret_cast<const float2*>(static_cast<const float*>(base) + idx);
+    }
+}
+
+// One warp per (row, 64 value dims); lane s holds lse_s, each lane owns two
+// dims.  Every part's two values are loaded in a single round (all loads in
+// flight before the first product), so the kernel costs two memory latencies:
+// the normalisers, then the values.
+template <bool kBf16In>
 __global__ void __launch_bounds__(256) merge_warp_kernel(MergeParams p) {
     wait_for_producer(p.pdl);
     const int lane = threadIdx.x & 31;
     const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    if (gw >= p.rows * 4) return;
-    const int64_t row = gw >> 2;
-    const int chunk = (int)(gw & 3);
-    const int64_t col = (int64_t)chunk * 128 + lane * 4;
+    if (gw >= p.rows * 8) return;
+    const int64_t row = gw >> 3;
+    const int chunk = (int)(gw & 7);
+    const int64_t col = (int64_t)chunk * 64 + lane * 2;
 
     const float ls = (lane < p.S) ? p.part_lse[(int64_t)lane * p.rows + row] : -INFINITY;
     const float M = warp_max(ls);
     uint16_t* dst = p.out + row * kDv + col;
     if (M == -INFINITY) {
-        *reinterpret_cast<uint2*>(dst) = make_uint2(0u, 0u);
+        *reinterpret_cast<uint32_t*>(dst) = 0u;
         if (chunk == 0 && lane == 0 && p.lse) p.lse[row] = -INFINITY;
         return;
     }
     const float e = (ls == -INFINITY) ? 0.f : exp2f((ls - M) * kLog2e);
     const float sum = warp_sum(e);
-    const float w = e / sum;
-    // Eight parts per round: all eight loads are in flight before the first
-    // product, so a round costs one memory latency, not eight.
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = 0; s0 < p.S; s0 += 8) {
-        float ws[8];
-        float4 v[8];
+    const float w = e / sum;  // lanes >= S: 0
+    float ws[32];
+    float2 v[32];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            ws[j] = __shfl_sync(0xffffffffu, w, (s0 + j) & 31);
-            if (s0 + j >= p.S) ws[j] = 0.f;
-            v[j] = ws[j] != 0.f ? load4<kBf16In>(p.part_out, ((int64_t)(s0 + j) * p.rows + row) * kDv + col)
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            acc.x = fmaf(ws[j], v[j].x, acc.x);
-            acc.y = fmaf(ws[j], v[j].y, acc.y);
-            acc.z = fmaf(ws[j], v[j].z, acc.z);
-            acc.w = fmaf(ws[j], v[j].w, acc.w);
-        }
+    for (int s = 0; s < 32; ++s) {
+        ws[s] = __shfl_sync(0xffffffffu, w, s);
+        v[s] = ws[s] != 0.f ? load2<kBf16In>(p.part_out, ((int64_t)s * p.rows + row) * kDv + col)
+                            : make_float2(0.f, 0.f);
     }
-    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-    *reinterpret_cast<uint2*>(dst) =
-        make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int s = 0; s < 32; ++s) {
+        acc.x = fmaf(ws[s], v[s].x, acc.x);
+        acc.y = fmaf(ws[s], v[s].y, acc.y);
+    }
+    __nv_bfloat162 o = __floats2bfloat162_rn(acc.x, acc.y);
+    *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<uint32_t*>(&o);
     if (chunk == 0 && lane == 0 && p.lse) p.lse[row] = M + logf(sum);
 }
 
@@ -193,7 +187,7 @@ cudaError_t launch_with_pdl(K kernel, dim3 grid, dim3 block, cudaStream_t stream
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
     if (p.rows == 0) return cudaSuccess;
     if (p.S <= 32) {
-        const int64_t warps = p.rows * 4;
+        const int64_t warps = p.rows * 8;
         const dim3 grid((unsigned)((warps + 7) / 8));
         return p.in_bf16 ? launch_with_pdl(merge_warp_kernel<true>, grid, dim3(256), stream, p)
                          : launch_with_pdl(merge_warp_kernel<false>, grid, dim3(256), stream, p);

@@ -76,6 +76,7 @@ struct Smem {
     float red_m[kGroups][2][kNq][4];         // [group][iter parity][head][warp] tile maxima
     float red_l[kGroups][kNq][4];            // per group: end-of-loop normaliser partials
     float fin[kGroups][2][kNq];              // per group: final max / normaliser by head
+    float wrow[kGroups][kNq];                // final weight of each group's tile, by head
     float row_scale[kNq];                    // kv_scale * sm_scale * log2(e) * 2^-e
     int rowlim[kNq];                         // visible prefix per row; -1 = padding
     uint64_t full[kStages], empty[kStages];
@@ -786,20 +787,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 
         // ---- merge the warpgroups' running states; write the answer ----
-        // Warpgroups 1.. park their state in a page slot that no copy or MMA
-        // touches any more: the slot of their own last page, or an unused one.
-        auto park_of = [&](int gg) -> float* {
-            const int c = n_pages > gg ? (n_pages - gg + kGroups - 1) / kGroups : 0;
-            const int sl = c > 0 ? (gg + kGroups * (c - 1)) % kStages : kStages - gg;
-            return reinterpret_cast<float*>(S.slot[sl]);
-        };
-        const int t_in_g = 32 * quad + lane;
+        // Warpgroup 1 parks its tile as [row][512] fp32 in a page slot that no
+        // copy or MMA touches any more (the slot of its own last page, or an
+        // unused one); warpgroup 0 merges it with its own tile, still in
+        // registers, stages the answer rows in the next slot and sends them in
+        // one bulk copy (they are contiguous in global memory).
+        static_assert(kGroups == 2, "the staging slots assume two warpgroups");
+        const int sl_park = [&] {
+            const int c1 = n_pages > 1 ? (n_pages - 1 + kGroups - 1) / kGroups : 0;
+            return c1 > 0 ? (1 + kGroups * (c1 - 1)) % kStages : kStages - 1;
+        }();
+        float* park = reinterpret_cast<float*>(S.slot[sl_park]);
+        float* stage = reinterpret_cast<float*>(S.slot[(sl_park + 1) % kStages]);
+        __nv_bfloat16* stage_bf = reinterpret_cast<__nv_bfloat16*>(S.slot[(sl_park + 2) % kStages]);
         if (g > 0) {
-            float* park = park_of(g);
 #pragma unroll
             for (int c = 0; c < 4; ++c)
 #pragma unroll
-                for (int h = 0; h < kRows; ++h) park[(c * kRows + h) * 128 + t_in_g] = o[c][h];
+                for (int h = 0; h < kRows; ++h) park[h * kDv + 128 * c + d] = o[c][h];
             if (quad == 0 && lane < kNq) {
                 S.fin[g][0][lane] = m_run;
                 S.fin[g][1][lane] = l_run;
@@ -808,58 +813,77 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(&S.fin_bar);
         } else {
             const bool ok = __all_sync(0xffffffffu, wait_bounded(&S.fin_bar, 0, abort, p.err));
-            // lane h: merged max, weights of the groups, merged normaliser
-            float wg[kGroups], l = l_run;
-            wg[0] = 1.f;
-#pragma unroll
-            for (int gg = 1; gg < kGroups; ++gg) wg[gg] = 0.f;
-            if (lane < kNq && ok) {
-                float mn = m_run;
-#pragma unroll
-                for (int gg = 1; gg < kGroups; ++gg) mn = fmaxf(mn, S.fin[gg][0][lane]);
-                if (mn != NEG) {
-                    wg[0] = exp2f(m_run - mn);
-                    l = l_run * wg[0];
-#pragma unroll
-                    for (int gg = 1; gg < kGroups; ++gg) {
-                        wg[gg] = exp2f(S.fin[gg][0][lane] - mn);
-                        l += S.fin[gg][1][lane] * wg[gg];
+            const bool direct = p.n_splits == 1;
+            // lane h: the weight of each tile (normaliser and kv_scale folded in)
+            if (quad == 0 && lane < kNq) {
+                float mn = m_run, l = l_run, w0 = 1.f, w1 = 0.f;
+                if (ok) {
+                    const float m1 = S.fin[1][0][lane], l1 = S.fin[1][1][lane];
+                    mn = fmaxf(m_run, m1);
+                    if (mn != NEG) {
+                        w0 = exp2f(m_run - mn);
+                        w1 = exp2f(m1 - mn);
+                        l = l_run * w0 + l1 * w1;
                     }
-                    m_run = mn;
+                }
+                const float inv = (l > 0.f) ? kv_scale / l : 0.f;
+                S.wrow[0][lane] = w0 * inv;
+                S.wrow[1][lane] = w1 * inv;
+                if (lane < HT) {
+                    const float lse = (l > 0.f) ? (mn + log2f(l)) * kLn2 : -INFINITY;
+                    const int64_t grow = (int64_t)b * HT + lane;
+                    if (direct) {
+                        if (p.lse) p.lse[grow] = lse;
+                    } else {
+                        p.part_lse[(int64_t)split * p.B * HT + grow] = lse;
+                    }
                 }
             }
-            const bool direct = p.n_splits == 1;
+            asm volatile("bar.sync 1, 128;" ::: "memory");  // warpgroup 0: weights
+            const int n = HT * kDv;
+            // Every load first (the parked tile and the weights), then the
+            // products and the staging stores.
+            float pk[4][kRows], w0[kRows], w1[kRows];
 #pragma unroll
             for (int h = 0; h < kRows; ++h) {
-                float w[kGroups];
+                w0[h] = S.wrow[0][h];
+                w1[h] = S.wrow[1][h];
 #pragma unroll
-                for (int gg = 0; gg < kGroups; ++gg) w[gg] = __shfl_sync(0xffffffffu, wg[gg], h);
-                const float lh = __shfl_sync(0xffffffffu, l, h);
-                if (h >= HT) continue;
-                const int64_t grow = (int64_t)b * HT + h;
-                const float inv = (lh > 0.f) ? kv_scale / lh : 0.f;
+                for (int c = 0; c < 4; ++c) pk[c][h] = (ok && h < HT) ? park[h * kDv + 128 * c + d] : 0.f;
+            }
+#pragma unroll
+            for (int h = 0; h < kRows; ++h) {
+                if (h >= HT) break;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    float v = o[c][h] * w[0];
-#pragma unroll
-                    for (int gg = 1; gg < kGroups; ++gg)
-                        if (ok) v = fmaf(park_of(gg)[(c * kRows + h) * 128 + t_in_g], w[gg], v);
-                    v *= inv;
-                    if (direct) {
-                        __nv_bfloat16 bv = __float2bfloat16_rn(v);
-                        p.out[grow * kDv + 128 * c + d] = *reinterpret_cast<uint16_t*>(&bv);
-                    } else if (lh > 0.f) {
-                        p.part_out[((int64_t)split * p.B * HT + grow) * kDv + 128 * c + d] = v;
-                    }
+                    const float v = fmaf(pk[c][h], w1[h], o[c][h] * w0[h]);
+                    if (direct)
+                        stage_bf[h * kDv + 128 * c + d] = __float2bfloat16_rn(v);
+                    else
+                        stage[h * kDv + 128 * c + d] = v;
                 }
             }
-            if (quad == 0 && lane < HT && lane < kNq) {
-                const float lse = (l > 0.f) ? (m_run + log2f(l)) * kLn2 : -INFINITY;
-                const int64_t grow = (int64_t)b * HT + lane;
-                if (direct) {
-                    if (p.lse) p.lse[grow] = lse;
-                } else {
-                    p.part_lse[(int64_t)split * p.B * HT + grow] = lse;
+            fence_async_smem();  // staged rows: generic writes -> bulk-copy reads
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            void* dst = direct ? static_cast<void*>(p.out + (int64_t)b * HT * kDv)
+                               : static_cast<void*>(p.part_out + ((int64_t)split * p.B * HT + (int64_t)b * HT) * kDv);
+            const void* src = direct ? static_cast<const void*>(stage_bf) : static_cast<const void*>(stage);
+            const uint32_t bytes = static_cast<uint32_t>(n) * (direct ? 2u : 4u);
+            if ((reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+                if (tid == 128 && bytes > 0) {
+                    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                                     reinterpret_cast<uint64_t>(dst)),
+                                 "r"(smem_u32(src)), "r"(bytes)
+                                 : "memory");
+                    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+                }
+            } else {  // destination not 16-byte aligned: plain stores
+                for (int idx = tid - 128; idx < n; idx += 128) {
+                    if (direct)
+                        static_cast<__nv_bfloat16*>(dst)[idx] = stage_bf[idx];
+                    else
+                        static_cast<float*>(dst)[idx] = stage[idx];
                 }
             }
         }
