@@ -170,7 +170,7 @@ def run_ours(args):
     caches = [base.kv_cache] + [base.kv_cache.clone() for _ in range(n_copies - 1)]
     out = torch.empty((B, T, H, 512), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((B, T, H), dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream(dev)
+    stream = torch.cuda.Stream(dev)
 
     def step(i):
         L.mla_decode_paged(base.q, caches[i % n_copies], base.kv_scale, base.block_table,
@@ -190,16 +190,44 @@ def run_ours(args):
     barrier()
     assert L.mla_device_error() == 0
 
+    # ---- the step as a serving loop runs it: a CUDA graph of gsteps calls ----
+    # (one call per cache copy, repeated; captured after the warm-up, so that the
+    # library's per-stream scratch already exists)
+    gsteps = n_copies * max(1, -(-16 // n_copies))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(gsteps):
+            step(i)
+    with torch.cuda.stream(stream):
+        graph.replay()
+    barrier()
+    assert L.mla_device_error() == 0
+
     # ---- main timed region: exactly K steps ----
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_rep, n_rem = divmod(args.steps, gsteps)
     with ClockSampler(local) as clk:
         barrier()
         ev0.record(stream)
-        for i in range(args.steps):
+        with torch.cuda.stream(stream):
+            for _ in range(n_rep):
+                graph.replay()
+        for i in range(n_rem):
             step(i)
         ev1.record(stream)
         barrier()
     ms_total = ev0.elapsed_time(ev1)
+    assert L.mla_device_error() == 0
+
+    # ---- the same steps as individual API calls (host launch cost included) ----
+    kdirect = min(args.steps, 2000)
+    barrier()
+    ev0.record(stream)
+    for i in range(kdirect):
+        step(i)
+    ev1.record(stream)
+    barrier()
+    ms_direct = ev0.elapsed_time(ev1) / kdirect
     if world > 1:
         t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -247,14 +275,15 @@ def run_ours(args):
         ksteps = min(args.steps, 1000)
 
         def e2e_step(i):
-            dq.copy_(hq, non_blocking=True)
-            dbt.copy_(hbt, non_blocking=True)
-            dsl.copy_(hsl, non_blocking=True)
-            dks.copy_(hks, non_blocking=True)
-            L.mla_decode_paged(dq, caches[i % n_copies], dks, dbt, dsl, n_splits, base.sm_scale,
-                               out, lse, stream)
-            hout.copy_(out, non_blocking=True)
-            hlse.copy_(lse, non_blocking=True)
+            with torch.cuda.stream(stream):  # copies and decode in one stream order
+                dq.copy_(hq, non_blocking=True)
+                dbt.copy_(hbt, non_blocking=True)
+                dsl.copy_(hsl, non_blocking=True)
+                dks.copy_(hks, non_blocking=True)
+                L.mla_decode_paged(dq, caches[i % n_copies], dks, dbt, dsl, n_splits, base.sm_scale,
+                                   out, lse, stream)
+                hout.copy_(out, non_blocking=True)
+                hlse.copy_(lse, non_blocking=True)
             stream.synchronize()
 
         for i in range(3):
@@ -292,7 +321,12 @@ def run_ours(args):
                        "page": 64, "kv_bytes_per_step": kv_bytes, "n_splits": n_eff,
                        "chunk_pages": chunk, "l2": f"{n_copies} rotating cache copies "
                        f"({n_copies * base.kv_cache.numel() / 1e6:.0f} MB > L2 {l2 / 1e6:.0f} MB)",
-                       "kernel_family": family},
+                       "kernel_family": family,
+                       "timing": f"CUDA-graph replays of {gsteps} mla_decode_paged calls "
+                                 f"({n_rep} replays + {n_rem} direct calls)"},
+            "direct_calls": {"value": round(world * kv_bytes / (ms_direct * 1e-3) / 1e9, 1),
+                             "unit": "GB/s", "ms_per_step": round(ms_direct, 5), "steps": kdirect,
+                             "note": "one host API call per step, no graph"},
             "decode_steps_per_s": round(steps_per_s, 1),
             "frac_of_8TBps": round(value / HBM_NOMINAL_GBS, 4),
             "roofline": roofline,

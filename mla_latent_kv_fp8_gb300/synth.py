@@ -246,6 +246,9 @@ def workload_case(name, device="cpu", reduced=False):
     if name == "long":
         L = 20000 + 13 if reduced else 393216
         return make_decode_case(seed, [L], 12, 1, device=device)
+    if name == "dcp_shard":  # one DCP shard as decoded locally: out + lse over its positions
+        L = 300 + 11 if reduced else 17750
+        return make_decode_case(seed, [L] * (2 if reduced else 32), 96, 1, device=device)
     if name == "ragged":
         lens = ragged_lens(seed, 16, 64, 3000) if reduced else ragged_lens(seed)
         return make_decode_case(seed, lens, 12, 1, device=device)

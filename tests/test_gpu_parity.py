@@ -92,7 +92,7 @@ def oracle_rows(case, reqs, heads):
 @pytest.mark.parametrize("name,n_splits", [
     ("tiny", 4), ("tiny", 1), ("tp8_batch", 0), ("tp8_batch", 1), ("tp8_batch", 3),
     ("tp8_batch", 7), ("verify", 0), ("verify", 5), ("long", 0), ("long", 200),
-    ("ragged", 0), ("ragged", 9)])
+    ("ragged", 0), ("ragged", 9), ("dcp_shard", 0), ("dcp_shard", 2)])
 def test_reduced_workloads_match_oracle(L, impl, name, n_splits):
     case = synth.workload_case(name, reduced=True)
     out, lse = supported(L, impl, case.to("cuda"), n_splits)
