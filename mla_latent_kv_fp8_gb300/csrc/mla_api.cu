@@ -184,9 +184,10 @@ int32_t mla_set_impl(int32_t impl) { return g_impl.exchange(impl); }
 int32_t mla_last_decode_impl(void) { return t_last_impl; }
 
 int32_t mla_auto_splits(int32_t B, int32_t T, int32_t H, int32_t max_pages, int32_t sm_count) {
-    (void)T;
-    (void)H;
     if (B <= 0 || max_pages <= 2) return 1;
+    // Rows (t, h) beyond 16 take a cluster of ceil(rows / 16) CTAs per unit.
+    const int64_t rows = (int64_t)(T > 0 ? T : 1) * (H > 0 ? H : 1);
+    const int64_t G = rows > 16 ? ceil_div(rows, 16) : 1;
     if (sm_count <= 0) {
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -195,8 +196,9 @@ int32_t mla_auto_splits(int32_t B, int32_t T, int32_t H, int32_t max_pages, int3
             sm_count = 148;
         }
     }
-    // One full wave of (request, partition) units, partitions of >= 2 pages.
-    int64_t s = ceil_div(sm_count, B);
+    // One full wave of (request, partition) units, partitions of >= 2 pages; two
+    // waves of clusters, whose placement leaves some SMs idle in each wave.
+    int64_t s = G == 1 ? ceil_div(sm_count, B) : ceil_div(2 * (int64_t)sm_count, B * G);
     const int64_t most = ceil_div(max_pages, 2);
     if (s > most) s = most;
     if (s < 1) s = 1;

@@ -8,7 +8,8 @@
 //
 // Design (GB300-first):
 //   * The FP8 codes are MMA operands as they sit in the cache: every 64-position
-//     page is bulk-copied by TMA (nine 64x64-byte boxes, 64-byte swizzle) into a
+//     page is bulk-copied by one TMA instruction (a 3-D box that lands as nine
+//     64x64-byte tiles with 64-byte swizzle) into a
 //     5-deep shared-memory ring and consumed by tcgen05.mma kind::f8f6f4 with no
 //     dequantisation pass.  kv_scale is folded into the score scale and the
 //     output scale.
@@ -53,6 +54,7 @@ constexpr int kThreads = 128 + 128 * kGroups;
 constexpr int kStages = 5;                   // page slots in the TMA ring
 constexpr int kNq = 16;                      // rows (t, h) per CTA, padded
 constexpr int kNqk = 2 * kNq;                // MMA N: q1 rows | q2 rows (and p1 | p2)
+constexpr int kMaxClusterRows = 8 * kNq;     // rows beyond 16: clusters of up to 8 CTAs
 constexpr int kSlotBytes = kPage * kDqk;     // 36,864: one page
 constexpr int kBoxBytes = kPage * 64;        // 4,096: 64 positions x 64 dims
 constexpr int kBoxes = kDqk / 64;            // 9
@@ -77,9 +79,11 @@ struct Smem {
     float red_l[kGroups][kNq][4];            // per group: end-of-loop normaliser partials
     float fin[kGroups][2][kNq];              // per group: final max / normaliser by head
     float wrow[kGroups][kNq];                // final weight of each group's tile, by head
-    float row_scale[kNq];                    // kv_scale * sm_scale * log2(e) * 2^-e
-    int rowlim[kNq];                         // visible prefix per row; -1 = padding
+    alignas(16) float row_scale[kNq];        // kv_scale * sm_scale * log2(e) * 2^-e
+    alignas(16) int rowlim[kNq];             // visible prefix per row; -1 = padding
+    alignas(16) float rref[4 * kGroups][kNq];  // per attention warp: reference of each head
     uint64_t full[kStages], empty[kStages];
+    uint64_t cempty[kStages];                // cluster leader: every CTA's slot awaits the page
     uint64_t s_full[kSBufs], s_empty[kSBufs];
     uint64_t p_full[kGroups][2];             // group's probabilities of its page are ready
     uint64_t pv_done[kGroups][2];            // group's PV of its page k done (buffer k & 1)
@@ -153,12 +157,12 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     return __all_sync(0xffffffffu, wait_bounded(bar, parity, abort, err));
 }
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            uint64_t* bar) {
+// One whole page (see encode_cache_map): a single copy instruction.
+__device__ __forceinline__ void tma_load_page(uint32_t dst, const CUtensorMap* map, int row, uint64_t* bar) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row), "r"(0), "r"(smem_u32(bar))
         : "memory");
 }
 
@@ -248,6 +252,47 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 }
 __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// ---- thread-block cluster helpers (rows beyond 16 are spread over a cluster) ----
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Address of the same shared-memory object in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// All threads of all CTAs of the cluster.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// One whole page, delivered to the same offset in every CTA of `mask` and
+// completing bytes on each one's barrier at the same offset.
+__device__ __forceinline__ void tma_load_page_multicast(uint32_t dst, const CUtensorMap* map, int row,
+                                                        uint64_t* bar, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row), "r"(0), "r"(smem_u32(bar)), "h"(mask)
+        : "memory");
 }
 
 // True in exactly one lane of a converged warp.
@@ -344,8 +389,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int split = blockIdx.x, b = blockIdx.y;
     const int HT = p.H * p.T;
+    // More than 16 rows: a cluster of G CTAs, CTA r taking rows [16r, 16r + 16)
+    // of every page, which the cluster leader copies once into all of them.
+    const int G = HT > kNq ? (HT + kNq - 1) / kNq : 1;
+    const int crank = G > 1 ? static_cast<int>(cluster_rank()) : 0;
+    const int split = blockIdx.x / G, b = blockIdx.y;
+    const int r0 = kNq * crank;                  // first (t, h) row of this CTA
+    const int HTc = min(kNq, HT - r0);           // rows of this CTA
     volatile int* abort = &S.abort;
 
     // Global loads that depend only on the launch indices go out together,
@@ -363,11 +414,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int rr = 0; rr < 2; ++rr) {
             const int r = warp - 1 + (kThreads / 32 - 1) * rr;
-            const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)b * HT + r) * kDqk);
+            const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)b * HT + r0 + r) * kDqk);
 #pragma unroll
             for (int k = 0; k < 3; ++k) {
                 const int c = lane + 32 * k;  // 16-byte chunk: 8 bf16 values
-                qv[rr][k] = (r < kNq && r < HT && c < kDqk / 8) ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+                qv[rr][k] = (r < kNq && r < HTc && c < kDqk / 8) ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
             }
         }
     }
@@ -386,6 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&S.full[s], 1);
             mbar_init(&S.empty[s], 1);
+            mbar_init(&S.cempty[s], G);
         }
         for (int i = 0; i < kSBufs; ++i) {
             mbar_init(&S.s_full[i], 1);
@@ -406,28 +458,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     __syncthreads();  // barriers initialised
+    if (G > 1) cluster_sync_all();  // ... in every CTA of the cluster, before any copy or remote arrive
     // The producer (warp 0) starts the first copies at once and takes no part in
     // the rest of the set-up: issuing a copy can stall its thread for a long
     // time, and the other warps prepare the query and TMEM meanwhile.
     int issued = 0;
-    auto issue_page = [&](int i, int32_t pid) {  // one thread
+    // Page i into slot i % kStages (one thread).  In a cluster every CTA arms its
+    // own barrier and reports its free slot to the leader, which copies the page
+    // into all of them once every slot is free.  False: the leader gave up.
+    auto issue_page = [&](int i, int32_t pid) -> bool {
         const int s = i % kStages;
         if (pid < 0 || pid >= p.num_pages) {
-            atomicCAS(p.err, 0, kErrPageRange);
+            if (crank == 0) atomicCAS(p.err, 0, kErrPageRange);
             pid = 0;  // load a valid page; the softmax masks and zeroes it
         }
         mbar_expect_tx(&S.full[s], kSlotBytes);
         const uint32_t dst = smem_u32(S.slot[s]);
-#pragma unroll
-        for (int j = 0; j < kBoxes; ++j) tma_load_2d(dst + j * kBoxBytes, &tmap, 64 * j, pid * kPage, &S.full[s]);
+        if (G == 1) {
+            tma_load_page(dst, &tmap, pid * kPage, &S.full[s]);
+            return true;
+        }
+        if (crank != 0) {
+            mbar_arrive_remote(mapa_shared(smem_u32(&S.cempty[s]), 0));
+            return true;
+        }
+        mbar_arrive(&S.cempty[s]);
+        const uint64_t t0 = global_ns();
+        for (uint32_t it = 0; !mbar_try_wait_cluster(&S.cempty[s], (i / kStages) & 1); ++it) {
+            if ((it & 127u) == 127u && (*abort || global_ns() - t0 > kTimeoutNs)) {
+                *abort = 1;
+                atomicCAS(p.err, 0, kErrWaitTimeout);
+                return false;
+            }
+        }
+        tma_load_page_multicast(dst, &tmap, pid * kPage, &S.full[s], static_cast<uint16_t>((1u << G) - 1u));
+        return true;
     };
     if (warp == 0 && n_pages > 0) {
         const int first = min(kStages, n_pages);  // fresh slots: nothing to wait for
         for (int i = 0; i < first; ++i) {
             const int32_t pid = __shfl_sync(0xffffffffu, pid_cur, i);
-            if (lane == 0) issue_page(i, pid);
+            int ok = 1;
+            if (lane == 0) ok = issue_page(i, pid) ? 1 : 0;
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            issued = i + 1;
         }
-        issued = first;
         __syncwarp();
     }
     if (warp == 1) {
@@ -442,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int rr = 0; rr < 2; ++rr) {
         const int r = warp - 1 + (kThreads / 32 - 1) * rr;
         if (warp == 0 || r >= kNq) continue;
-        if (r < HT) {
+        if (r < HTc) {
             const uint4* v = qv[rr];
             float amax = 0.f;
 #pragma unroll
@@ -480,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (lane == 0) {
                 S.row_scale[r] = kv_scale * p.sm_scale_log2 * ldexpf(1.f, -e);
-                S.rowlim[r] = (L == 0) ? 0 : L - p.T + 1 + r / p.H;
+                S.rowlim[r] = (L == 0) ? 0 : L - p.T + 1 + (r0 + r) / p.H;
             }
         } else {
             for (int c = lane; c < kDqk / 8; c += 32) {
@@ -503,25 +578,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ======================= TMA producer =======================
         if (n_pages > 0) {
-            for (int i = issued; i < n_pages; ++i) {
+            for (int i = issued; i < n_pages && !*abort; ++i) {
                 if ((i & 31) == 0) {  // next window of page ids; prefetch the one after
                     pid_cur = pid_nxt;
                     pid_nxt = i + 32 + lane < n_pages ? __ldg(bt_cta + i + 32 + lane) : 0;
                 }
                 const int32_t pid = __shfl_sync(0xffffffffu, pid_cur, i & 31);
                 if (!warp_wait(&S.empty[i % kStages], ((i / kStages) & 1) ^ 1, abort, p.err)) break;
-                if (lane == 0) issue_page(i, pid);
-                __syncwarp();
+                int ok = 1;
+                if (lane == 0) ok = issue_page(i, pid) ? 1 : 0;
+                if (!__shfl_sync(0xffffffffu, ok, 0)) break;
                 issued = i + 1;
             }
         }
         if (lane == 0 && n_pages > 0) {
-            // Drain: never leave with a copy in flight into this CTA's shared memory.
+            // Drain: never leave with a copy in flight into this CTA's shared memory
+            // (one deadline for all of them).
+            const uint64_t t0 = global_ns();
             for (int i = max(0, issued - kStages); i < issued; ++i) {
                 const int s = i % kStages;
                 const uint32_t par = (i / kStages) & 1;
-                if (mbar_try_wait(&S.full[s], par)) continue;
-                const uint64_t t0 = global_ns();
                 while (!mbar_try_wait(&S.full[s], par) && global_ns() - t0 < kTimeoutNs) {
                 }
             }
@@ -623,16 +699,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool causal = p.T > 1;             // for T = 1 the partition end bounds every row
         const uint32_t to = tmem + (static_cast<uint32_t>(32 * quad) << 16) + kOCol0 + 128 * g;
         const int32_t* bt = p.block_table + (int64_t)b * p.bt_stride + pg_begin;
+        // Per-head values that every lane needs (score scale, reference) are
+        // read from shared memory as four 16-byte vectors when used, which keeps
+        // them out of the register budget; each warp keeps its own copy of the
+        // references (identical across the group), so it updates them alone.
         float lp[kRows];                         // normaliser partials of this thread's positions
-        float r[kRows];                          // reference of each head (same in all lanes)
-        float rsc[kRows];                        // score scale of each row
-        float r_l = NEG;                         // lane h < kRows: r[h]
+        float r_l = NEG;                         // lane h < kRows: reference of head h
+        float* rref = S.rref[warp - 4];          // this warp's copy of the references
+        if (lane < kNq) rref[lane] = NEG;
+        __syncwarp();
 #pragma unroll
-        for (int h = 0; h < kRows; ++h) {
-            lp[h] = 0.f;
-            r[h] = NEG;
-            rsc[h] = S.row_scale[h];
-        }
+        for (int h = 0; h < kRows; ++h) lp[h] = 0.f;
         bool fail = false;
         int k = 0;
         int32_t pid_next = g < n_pages ? __ldg(bt + g) : 0;
@@ -657,11 +734,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&S.s_empty[sb]);
                 const bool in_part = has_row && page_ok && pos < p_end;
+                float rsc[16];
+                int lim[16];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float4 a4 = reinterpret_cast<const float4*>(S.row_scale)[j];
+                    rsc[4 * j] = a4.x, rsc[4 * j + 1] = a4.y, rsc[4 * j + 2] = a4.z, rsc[4 * j + 3] = a4.w;
+                    if (causal) {
+                        const int4 l4 = reinterpret_cast<const int4*>(S.rowlim)[j];
+                        lim[4 * j] = l4.x, lim[4 * j + 1] = l4.y, lim[4 * j + 2] = l4.z, lim[4 * j + 3] = l4.w;
+                    } else {
+                        lim[4 * j] = lim[4 * j + 1] = lim[4 * j + 2] = lim[4 * j + 3] = 0;
+                    }
+                }
                 float mine = NEG;  // lane h < kRows ends up with this warp's max of head h
 #pragma unroll
                 for (int h = 0; h < kRows; ++h) {
                     const float v = (__uint_as_float(r1[h]) + __uint_as_float(r2[h]) * 0.0625f) * rsc[h];
-                    s[h] = (in_part && (!causal || pos < S.rowlim[h])) ? v : NEG;
+                    s[h] = (in_part && (!causal || pos < lim[h])) ? v : NEG;
                     const float wm = warp_max_redux(s[h]);
                     mine = (lane == h) ? wm : mine;
                 }
@@ -682,11 +772,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float rn = need ? t - kShift : r_l;
                 const float a = need ? exp2f(r_l - rn) : 1.f;  // r_l = -inf: nothing to keep
                 r_l = rn;
+                if (lane < kNq) rref[lane] = rn;
+                __syncwarp();
                 float al[kRows];
 #pragma unroll
                 for (int h = 0; h < kRows; ++h) {
                     al[h] = __shfl_sync(0xffffffffu, a, h);
-                    r[h] = __shfl_sync(0xffffffffu, rn, h);
                     lp[h] *= al[h];
                 }
                 if (k > 0) {
@@ -714,6 +805,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Buffer kb was last read by this group's PV two pages ago.
             if (!fail && k >= 2) fail = !warp_wait(&S.pv_done[g][kb], ((k >> 1) - 1) & 1, abort, p.err);
             if (!fail) {
+                float r[16];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float4 a4 = reinterpret_cast<const float4*>(rref)[j];
+                    r[4 * j] = a4.x, r[4 * j + 1] = a4.y, r[4 * j + 2] = a4.z, r[4 * j + 3] = a4.w;
+                }
 #pragma unroll
                 for (int h = 0; h < kRows; ++h) {
                     s[h] = (s[h] == NEG) ? 0.f : exp2f(s[h] - r[h]);
@@ -829,9 +926,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float inv = (l > 0.f) ? kv_scale / l : 0.f;
                 S.wrow[0][lane] = w0 * inv;
                 S.wrow[1][lane] = w1 * inv;
-                if (lane < HT) {
+                if (lane < HTc) {
                     const float lse = (l > 0.f) ? (mn + log2f(l)) * kLn2 : -INFINITY;
-                    const int64_t grow = (int64_t)b * HT + lane;
+                    const int64_t grow = (int64_t)b * HT + r0 + lane;
                     if (direct) {
                         if (p.lse) p.lse[grow] = lse;
                     } else {
@@ -840,23 +937,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             asm volatile("bar.sync 1, 128;" ::: "memory");  // warpgroup 0: weights
-            const int n = HT * kDv;
+            const int n = HTc * kDv;
             // Every load first (the parked tile and the weights), then the
             // products and the staging stores.
-            float pk[4][kRows], w0[kRows], w1[kRows];
+            float w0[kRows], w1[kRows];
 #pragma unroll
             for (int h = 0; h < kRows; ++h) {
                 w0[h] = S.wrow[0][h];
                 w1[h] = S.wrow[1][h];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) pk[c][h] = (ok && h < HT) ? park[h * kDv + 128 * c + d] : 0.f;
             }
 #pragma unroll
-            for (int h = 0; h < kRows; ++h) {
-                if (h >= HT) break;
+            for (int c = 0; c < 4; ++c) {  // one 128-dim block at a time (register budget)
+                float pk[kRows];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const float v = fmaf(pk[c][h], w1[h], o[c][h] * w0[h]);
+                for (int h = 0; h < kRows; ++h) pk[h] = (ok && h < HTc) ? park[h * kDv + 128 * c + d] : 0.f;
+#pragma unroll
+                for (int h = 0; h < kRows; ++h) {
+                    if (h >= HTc) break;
+                    const float v = fmaf(pk[h], w1[h], o[c][h] * w0[h]);
                     if (direct)
                         stage_bf[h * kDv + 128 * c + d] = __float2bfloat16_rn(v);
                     else
@@ -865,8 +963,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             fence_async_smem();  // staged rows: generic writes -> bulk-copy reads
             asm volatile("bar.sync 1, 128;" ::: "memory");
-            void* dst = direct ? static_cast<void*>(p.out + (int64_t)b * HT * kDv)
-                               : static_cast<void*>(p.part_out + ((int64_t)split * p.B * HT + (int64_t)b * HT) * kDv);
+            const int64_t row0 = (int64_t)b * HT + r0;  // this CTA's first answer row
+            void* dst = direct ? static_cast<void*>(p.out + row0 * kDv)
+                               : static_cast<void*>(p.part_out + ((int64_t)split * p.B * HT + row0) * kDv);
             const void* src = direct ? static_cast<const void*>(stage_bf) : static_cast<const void*>(stage);
             const uint32_t bytes = static_cast<uint32_t>(n) * (direct ? 2u : 4u);
             if ((reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
@@ -896,6 +995,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
                      : "memory");
     }
+    // No CTA of a cluster leaves while the leader's copies may still target it.
+    if (G > 1) cluster_sync_all();
 }
 
 // ---------------------------------------------------------------- host side
@@ -916,16 +1017,19 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
     return fn;
 }
 
-// The cache viewed as a 2-D byte tensor [num_pages * 64 rows][576 cols]; boxes of
-// 64 rows x 64 bytes with 64-byte swizzle (the UMMA SWIZZLE_64B atom).
+// The cache viewed as a 3-D byte tensor: (64-byte column chunk offset, row =
+// page * 64 + position, chunk of the 576-byte row), strides 576 B (row) and
+// 64 B (chunk).  One box {64, 64, 9} is a whole page, landing in shared memory
+// as nine 64-position x 64-byte tiles (chunk-major) with 64-byte swizzle: the
+// UMMA SWIZZLE_64B K-major layout of each 64-dim slice of the page.
 cudaError_t encode_cache_map(CUtensorMap* map, const uint8_t* kv, int64_t num_pages) {
     auto fn = get_encode_fn();
     if (!fn) return cudaErrorNotSupported;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDqk), static_cast<cuuint64_t>(num_pages * kPage)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(kDqk)};
-    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kPage)};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(kv), dims, strides, box,
+    cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(num_pages * kPage), static_cast<cuuint64_t>(kBoxes)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(kDqk), 64};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kPage), static_cast<cuuint32_t>(kBoxes)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(kv), dims, strides, box,
                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
@@ -934,7 +1038,7 @@ cudaError_t encode_cache_map(CUtensorMap* map, const uint8_t* kv, int64_t num_pa
 }  // namespace
 
 bool tc_supports(const DecodeParams& p, int cc_major, int cc_minor) {
-    return cc_major == 10 && cc_minor == 3 && p.H * p.T <= kNq && p.num_pages >= 1 &&
+    return cc_major == 10 && cc_minor == 3 && p.H * p.T <= kMaxClusterRows && p.num_pages >= 1 &&
            p.num_pages * kPage < (1ll << 31);
 }
 
@@ -967,11 +1071,29 @@ cudaError_t launch_tc_decode(const DecodeParams& p, cudaStream_t stream, bool* h
 
     CUtensorMap map;
     if ((e = encode_cache_map(&map, p.kv, p.num_pages)) != cudaSuccess) return e;
-    dim3 grid(p.n_splits, p.B);
-    if (p.H * p.T <= 12)
-        tc_decode_kernel<12><<<grid, kThreads, sizeof(Smem) + 1024, stream>>>(map, p);
-    else
-        tc_decode_kernel<16><<<grid, kThreads, sizeof(Smem) + 1024, stream>>>(map, p);
+    const int HT = p.H * p.T;
+    if (HT <= 12) {
+        tc_decode_kernel<12><<<dim3(p.n_splits, p.B), kThreads, sizeof(Smem) + 1024, stream>>>(map, p);
+    } else if (HT <= kNq) {
+        tc_decode_kernel<16><<<dim3(p.n_splits, p.B), kThreads, sizeof(Smem) + 1024, stream>>>(map, p);
+    } else {
+        // a cluster of G CTAs (16 rows each) per (split, request)
+        const unsigned G = static_cast<unsigned>((HT + kNq - 1) / kNq);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(G * static_cast<unsigned>(p.n_splits), static_cast<unsigned>(p.B));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = sizeof(Smem) + 1024;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = G;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, tc_decode_kernel<16>, map, p);
+        if (e != cudaSuccess) return e;
+    }
     e = cudaGetLastError();
     if (e == cudaSuccess) *handled = true;
     return e;
