@@ -183,6 +183,8 @@ int32_t mla_set_impl(int32_t impl) { return g_impl.exchange(impl); }
 
 int32_t mla_last_decode_impl(void) { return t_last_impl; }
 
+constexpr int64_t kChunkCapPages = 256;  // 16,384 positions
+
 int32_t mla_auto_splits(int32_t B, int32_t T, int32_t H, int32_t max_pages, int32_t sm_count) {
     if (B <= 0 || max_pages <= 2) return 1;
     // Rows (t, h) beyond 16 take a cluster of ceil(rows / 16) CTAs per unit.
@@ -196,10 +198,26 @@ int32_t mla_auto_splits(int32_t B, int32_t T, int32_t H, int32_t max_pages, int3
             sm_count = 148;
         }
     }
-    // One full wave of (request, partition) units, partitions of >= 2 pages; two
-    // waves of clusters, whose placement leaves some SMs idle in each wave.
-    int64_t s = G == 1 ? ceil_div(sm_count, B) : ceil_div(2 * (int64_t)sm_count, B * G);
     const int64_t most = ceil_div(max_pages, 2);
+    int64_t s;
+    if (G == 1) {
+        s = ceil_div(sm_count, B);  // one full wave of (request, partition) units
+    } else {
+        // Clusters: about 90% of the SMs can hold whole clusters at once.  Pick
+        // the count that minimises waves x (pages per partition + a fixed cost
+        // of ~8 pages per CTA), assuming every request is max_pages long.
+        const int64_t M = (sm_count * 9 / 10) / G > 0 ? (sm_count * 9 / 10) / G : 1;
+        int64_t best = -1;
+        s = 1;
+        for (int64_t c = 1; c <= most && c <= 1024; ++c) {
+            const int64_t cost = ceil_div(B * c, M) * (ceil_div(max_pages, c) + 8);
+            if (best < 0 || cost < best) best = cost, s = c;
+        }
+    }
+    // Partitions of at most kChunkCapPages pages: in a batch of mixed lengths the
+    // longest request would otherwise bound the call (the host cannot see the
+    // lengths); partitions past a request's end cost a CTA that exits at once.
+    if (s < ceil_div(max_pages, kChunkCapPages)) s = ceil_div(max_pages, kChunkCapPages);
     if (s > most) s = most;
     if (s < 1) s = 1;
     // Snap to the count that equal even-page chunks actually produce.

@@ -431,6 +431,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int p_begin = pg_begin * kPage;
     const int p_end = min(L, p_begin + p.chunk_pages * kPage);
     const int n_pages = p_end > p_begin ? (p_end - p_begin + kPage - 1) / kPage : 0;
+    if (n_pages == 0) {
+        // None of this request's history falls in this partition (every CTA of a
+        // cluster agrees): leave before any set-up.  Its rows get lse = -inf, a
+        // partial the merge skips, or, unsplit, out = 0 and lse = -inf.
+        const int64_t row0 = (int64_t)b * HT + r0;
+        if (p.n_splits == 1) {
+            for (int idx = tid; idx < HTc * kDv; idx += kThreads) p.out[row0 * kDv + idx] = 0;
+            if (p.lse)
+                for (int idx = tid; idx < HTc; idx += kThreads) p.lse[row0 + idx] = -INFINITY;
+        } else {
+            for (int idx = tid; idx < HTc; idx += kThreads)
+                p.part_lse[(int64_t)split * p.B * HT + row0 + idx] = -INFINITY;
+        }
+        return;
+    }
 
     // ---------------- set-up: barriers, TMEM, query operand ----------------
     if (tid == 0) {
@@ -699,17 +714,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool causal = p.T > 1;             // for T = 1 the partition end bounds every row
         const uint32_t to = tmem + (static_cast<uint32_t>(32 * quad) << 16) + kOCol0 + 128 * g;
         const int32_t* bt = p.block_table + (int64_t)b * p.bt_stride + pg_begin;
-        // Per-head values that every lane needs (score scale, reference) are
-        // read from shared memory as four 16-byte vectors when used, which keeps
-        // them out of the register budget; each warp keeps its own copy of the
-        // references (identical across the group), so it updates them alone.
+        // Per-head values that every lane needs (score scale, reference): with
+        // 12 rows they stay in registers; with 16 they are read from shared
+        // memory as four 16-byte vectors when used, which keeps the 16-row
+        // variant within the register budget.  Each warp keeps its own copy of
+        // the references (identical across the group), so it updates them alone.
+        constexpr bool kRegRows = kRows <= 12;
         float lp[kRows];                         // normaliser partials of this thread's positions
         float r_l = NEG;                         // lane h < kRows: reference of head h
-        float* rref = S.rref[warp - 4];          // this warp's copy of the references
+        float r_reg[kRows], rsc_reg[kRows];      // kRegRows only
+        float* rref = S.rref[warp - 4];          // this warp's copy of the references (16 rows)
         if (lane < kNq) rref[lane] = NEG;
         __syncwarp();
 #pragma unroll
-        for (int h = 0; h < kRows; ++h) lp[h] = 0.f;
+        for (int h = 0; h < kRows; ++h) {
+            lp[h] = 0.f;
+            r_reg[h] = NEG;
+            rsc_reg[h] = kRegRows ? S.row_scale[h] : 0.f;
+        }
         bool fail = false;
         int k = 0;
         int32_t pid_next = g < n_pages ? __ldg(bt + g) : 0;
@@ -738,8 +760,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int lim[16];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const float4 a4 = reinterpret_cast<const float4*>(S.row_scale)[j];
-                    rsc[4 * j] = a4.x, rsc[4 * j + 1] = a4.y, rsc[4 * j + 2] = a4.z, rsc[4 * j + 3] = a4.w;
+                    if constexpr (kRegRows) {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) rsc[4 * j + u] = 4 * j + u < kRows ? rsc_reg[(4 * j + u) % kRows] : 0.f;
+                    } else {
+                        const float4 a4 = reinterpret_cast<const float4*>(S.row_scale)[j];
+                        rsc[4 * j] = a4.x, rsc[4 * j + 1] = a4.y, rsc[4 * j + 2] = a4.z, rsc[4 * j + 3] = a4.w;
+                    }
                     if (causal) {
                         const int4 l4 = reinterpret_cast<const int4*>(S.rowlim)[j];
                         lim[4 * j] = l4.x, lim[4 * j + 1] = l4.y, lim[4 * j + 2] = l4.z, lim[4 * j + 3] = l4.w;
@@ -772,12 +799,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float rn = need ? t - kShift : r_l;
                 const float a = need ? exp2f(r_l - rn) : 1.f;  // r_l = -inf: nothing to keep
                 r_l = rn;
-                if (lane < kNq) rref[lane] = rn;
-                __syncwarp();
+                if constexpr (!kRegRows) {
+                    if (lane < kNq) rref[lane] = rn;
+                    __syncwarp();
+                }
                 float al[kRows];
 #pragma unroll
                 for (int h = 0; h < kRows; ++h) {
                     al[h] = __shfl_sync(0xffffffffu, a, h);
+                    if constexpr (kRegRows) r_reg[h] = __shfl_sync(0xffffffffu, rn, h);
                     lp[h] *= al[h];
                 }
                 if (k > 0) {
@@ -808,8 +838,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float r[16];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const float4 a4 = reinterpret_cast<const float4*>(rref)[j];
-                    r[4 * j] = a4.x, r[4 * j + 1] = a4.y, r[4 * j + 2] = a4.z, r[4 * j + 3] = a4.w;
+                    if constexpr (kRegRows) {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) r[4 * j + u] = 4 * j + u < kRows ? r_reg[(4 * j + u) % kRows] : 0.f;
+                    } else {
+                        const float4 a4 = reinterpret_cast<const float4*>(rref)[j];
+                        r[4 * j] = a4.x, r[4 * j + 1] = a4.y, r[4 * j + 2] = a4.z, r[4 * j + 3] = a4.w;
+                    }
                 }
 #pragma unroll
                 for (int h = 0; h < kRows; ++h) {
@@ -946,19 +981,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 w0[h] = S.wrow[0][h];
                 w1[h] = S.wrow[1][h];
             }
+            // All loads of a round first: the whole parked tile with 12 rows, one
+            // 128-dim block at a time with 16 (register budget).
+            constexpr int kRounds = kRows <= 12 ? 1 : 4;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {  // one 128-dim block at a time (register budget)
-                float pk[kRows];
+            for (int c0 = 0; c0 < 4; c0 += 4 / kRounds) {
+                float pk[4 / kRounds][kRows];
 #pragma unroll
-                for (int h = 0; h < kRows; ++h) pk[h] = (ok && h < HTc) ? park[h * kDv + 128 * c + d] : 0.f;
+                for (int cc = 0; cc < 4 / kRounds; ++cc)
 #pragma unroll
-                for (int h = 0; h < kRows; ++h) {
-                    if (h >= HTc) break;
-                    const float v = fmaf(pk[h], w1[h], o[c][h] * w0[h]);
-                    if (direct)
-                        stage_bf[h * kDv + 128 * c + d] = __float2bfloat16_rn(v);
-                    else
-                        stage[h * kDv + 128 * c + d] = v;
+                    for (int h = 0; h < kRows; ++h)
+                        pk[cc][h] = (ok && h < HTc) ? park[h * kDv + 128 * (c0 + cc) + d] : 0.f;
+#pragma unroll
+                for (int cc = 0; cc < 4 / kRounds; ++cc) {
+                    const int c = c0 + cc;
+#pragma unroll
+                    for (int h = 0; h < kRows; ++h) {
+                        if (h >= HTc) break;
+                        const float v = fmaf(pk[cc][h], w1[h], o[c][h] * w0[h]);
+                        if (direct)
+                            stage_bf[h * kDv + 128 * c + d] = __float2bfloat16_rn(v);
+                        else
+                            stage[h * kDv + 128 * c + d] = v;
+                    }
                 }
             }
             fence_async_smem();  // staged rows: generic writes -> bulk-copy reads
