@@ -168,9 +168,9 @@ mla_status_t mla_decode_paged_noalloc(const mla_tensor_t *q, const mla_tensor_t 
  * partitions per request that B * splits fills every SM of the device
  * (at least one full wave), with at least 2 pages (128 positions) each.
  * When H * T > 16 every (request, partition) unit takes ceil(H * T / 16)
- * SMs (a thread-block cluster); the count then minimises the number of waves
- * of clusters times the partition length.  Partitions never exceed 256 pages
- * (16,384 positions), so that in a batch of mixed lengths the longest request
+ * CTAs (16 rows each); the count then minimises the number of waves of CTAs
+ * times the partition length.  Partitions never exceed 160 pages
+ * (10,240 positions), so that in a batch of mixed lengths the longest request
  * does not bound the call.
  * Pure host function; sm_count <= 0 means "query the current device". */
 int32_t mla_auto_splits(int32_t B, int32_t T, int32_t H, int32_t max_pages, int32_t sm_count);

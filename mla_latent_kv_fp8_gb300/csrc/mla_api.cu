@@ -183,11 +183,11 @@ int32_t mla_set_impl(int32_t impl) { return g_impl.exchange(impl); }
 
 int32_t mla_last_decode_impl(void) { return t_last_impl; }
 
-constexpr int64_t kChunkCapPages = 256;  // 16,384 positions
+constexpr int64_t kChunkCapPages = 160;  // 10,240 positions
 
 int32_t mla_auto_splits(int32_t B, int32_t T, int32_t H, int32_t max_pages, int32_t sm_count) {
     if (B <= 0 || max_pages <= 2) return 1;
-    // Rows (t, h) beyond 16 take a cluster of ceil(rows / 16) CTAs per unit.
+    // Rows (t, h) beyond 16 take ceil(rows / 16) CTAs per unit.
     const int64_t rows = (int64_t)(T > 0 ? T : 1) * (H > 0 ? H : 1);
     const int64_t G = rows > 16 ? ceil_div(rows, 16) : 1;
     if (sm_count <= 0) {
@@ -203,14 +203,13 @@ int32_t mla_auto_splits(int32_t B, int32_t T, int32_t H, int32_t max_pages, int3
     if (G == 1) {
         s = ceil_div(sm_count, B);  // one full wave of (request, partition) units
     } else {
-        // Clusters: about 90% of the SMs can hold whole clusters at once.  Pick
-        // the count that minimises waves x (pages per partition + a fixed cost
-        // of ~8 pages per CTA), assuming every request is max_pages long.
-        const int64_t M = (sm_count * 9 / 10) / G > 0 ? (sm_count * 9 / 10) / G : 1;
+        // G CTAs per unit: pick the count that minimises waves of CTAs x (pages
+        // per partition + a fixed cost of ~8 pages per CTA), assuming every
+        // request is max_pages long.
         int64_t best = -1;
         s = 1;
         for (int64_t c = 1; c <= most && c <= 1024; ++c) {
-            const int64_t cost = ceil_div(B * c, M) * (ceil_div(max_pages, c) + 8);
+            const int64_t cost = ceil_div(B * c * G, sm_count) * (ceil_div(max_pages, c) + 8);
             if (best < 0 || cost < best) best = cost, s = c;
         }
     }

@@ -54,7 +54,7 @@ constexpr int kThreads = 128 + 128 * kGroups;
 constexpr int kStages = 5;                   // page slots in the TMA ring
 constexpr int kNq = 16;                      // rows (t, h) per CTA, padded
 constexpr int kNqk = 2 * kNq;                // MMA N: q1 rows | q2 rows (and p1 | p2)
-constexpr int kMaxClusterRows = 8 * kNq;     // rows beyond 16: clusters of up to 8 CTAs
+constexpr int kMaxRowsTc = 8 * kNq;          // rows beyond 16: up to 8 CTAs per partition
 constexpr int kSlotBytes = kPage * kDqk;     // 36,864: one page
 constexpr int kBoxBytes = kPage * 64;        // 4,096: 64 positions x 64 dims
 constexpr int kBoxes = kDqk / 64;            // 9
@@ -83,7 +83,6 @@ struct Smem {
     alignas(16) int rowlim[kNq];             // visible prefix per row; -1 = padding
     alignas(16) float rref[4 * kGroups][kNq];  // per attention warp: reference of each head
     uint64_t full[kStages], empty[kStages];
-    uint64_t cempty[kStages];                // cluster leader: every CTA's slot awaits the page
     uint64_t s_full[kSBufs], s_empty[kSBufs];
     uint64_t p_full[kGroups][2];             // group's probabilities of its page are ready
     uint64_t pv_done[kGroups][2];            // group's PV of its page k done (buffer k & 1)
@@ -254,47 +253,6 @@ __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// ---- thread-block cluster helpers (rows beyond 16 are spread over a cluster) ----
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-// Address of the same shared-memory object in CTA `rank` of this cluster.
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-    return r;
-}
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// All threads of all CTAs of the cluster.
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// One whole page, delivered to the same offset in every CTA of `mask` and
-// completing bytes on each one's barrier at the same offset.
-__device__ __forceinline__ void tma_load_page_multicast(uint32_t dst, const CUtensorMap* map, int row,
-                                                        uint64_t* bar, uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row), "r"(0), "r"(smem_u32(bar)), "h"(mask)
-        : "memory");
-}
-
 // True in exactly one lane of a converged warp.
 __device__ __forceinline__ bool elect_one() {
     uint32_t pred;
@@ -390,10 +348,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int HT = p.H * p.T;
-    // More than 16 rows: a cluster of G CTAs, CTA r taking rows [16r, 16r + 16)
-    // of every page, which the cluster leader copies once into all of them.
+    // More than 16 rows: G = ceil(H*T / 16) CTAs per (partition, request), CTA
+    // r taking rows [16r, 16r + 16) of every page.  They are adjacent in the
+    // grid, so they run at the same time and all but the first read each page
+    // from L2 (HBM still sees each page about once).
     const int G = HT > kNq ? (HT + kNq - 1) / kNq : 1;
-    const int crank = G > 1 ? static_cast<int>(cluster_rank()) : 0;
+    const int crank = G > 1 ? static_cast<int>(blockIdx.x % G) : 0;
     const int split = blockIdx.x / G, b = blockIdx.y;
     const int r0 = kNq * crank;                  // first (t, h) row of this CTA
     const int HTc = min(kNq, HT - r0);           // rows of this CTA
@@ -432,9 +392,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int p_end = min(L, p_begin + p.chunk_pages * kPage);
     const int n_pages = p_end > p_begin ? (p_end - p_begin + kPage - 1) / kPage : 0;
     if (n_pages == 0) {
-        // None of this request's history falls in this partition (every CTA of a
-        // cluster agrees): leave before any set-up.  Its rows get lse = -inf, a
-        // partial the merge skips, or, unsplit, out = 0 and lse = -inf.
+        // None of this request's history falls in this partition: leave before
+        // any set-up.  Its rows get lse = -inf, a partial the merge skips, or,
+        // unsplit, out = 0 and lse = -inf.
         const int64_t row0 = (int64_t)b * HT + r0;
         if (p.n_splits == 1) {
             for (int idx = tid; idx < HTc * kDv; idx += kThreads) p.out[row0 * kDv + idx] = 0;
@@ -452,7 +412,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&S.full[s], 1);
             mbar_init(&S.empty[s], 1);
-            mbar_init(&S.cempty[s], G);
         }
         for (int i = 0; i < kSBufs; ++i) {
             mbar_init(&S.s_full[i], 1);
@@ -473,51 +432,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     __syncthreads();  // barriers initialised
-    if (G > 1) cluster_sync_all();  // ... in every CTA of the cluster, before any copy or remote arrive
     // The producer (warp 0) starts the first copies at once and takes no part in
     // the rest of the set-up: issuing a copy can stall its thread for a long
     // time, and the other warps prepare the query and TMEM meanwhile.
     int issued = 0;
-    // Page i into slot i % kStages (one thread).  In a cluster every CTA arms its
-    // own barrier and reports its free slot to the leader, which copies the page
-    // into all of them once every slot is free.  False: the leader gave up.
-    auto issue_page = [&](int i, int32_t pid) -> bool {
+    // Page i into slot i % kStages (one thread).
+    auto issue_page = [&](int i, int32_t pid) {
         const int s = i % kStages;
         if (pid < 0 || pid >= p.num_pages) {
             if (crank == 0) atomicCAS(p.err, 0, kErrPageRange);
             pid = 0;  // load a valid page; the softmax masks and zeroes it
         }
         mbar_expect_tx(&S.full[s], kSlotBytes);
-        const uint32_t dst = smem_u32(S.slot[s]);
-        if (G == 1) {
-            tma_load_page(dst, &tmap, pid * kPage, &S.full[s]);
-            return true;
-        }
-        if (crank != 0) {
-            mbar_arrive_remote(mapa_shared(smem_u32(&S.cempty[s]), 0));
-            return true;
-        }
-        mbar_arrive(&S.cempty[s]);
-        const uint64_t t0 = global_ns();
-        for (uint32_t it = 0; !mbar_try_wait_cluster(&S.cempty[s], (i / kStages) & 1); ++it) {
-            if ((it & 127u) == 127u && (*abort || global_ns() - t0 > kTimeoutNs)) {
-                *abort = 1;
-                atomicCAS(p.err, 0, kErrWaitTimeout);
-                return false;
-            }
-        }
-        tma_load_page_multicast(dst, &tmap, pid * kPage, &S.full[s], static_cast<uint16_t>((1u << G) - 1u));
-        return true;
+        tma_load_page(smem_u32(S.slot[s]), &tmap, pid * kPage, &S.full[s]);
     };
     if (warp == 0 && n_pages > 0) {
         const int first = min(kStages, n_pages);  // fresh slots: nothing to wait for
         for (int i = 0; i < first; ++i) {
             const int32_t pid = __shfl_sync(0xffffffffu, pid_cur, i);
-            int ok = 1;
-            if (lane == 0) ok = issue_page(i, pid) ? 1 : 0;
-            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-            issued = i + 1;
+            if (lane == 0) issue_page(i, pid);
         }
+        issued = first;
         __syncwarp();
     }
     if (warp == 1) {
@@ -593,16 +528,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ======================= TMA producer =======================
         if (n_pages > 0) {
-            for (int i = issued; i < n_pages && !*abort; ++i) {
+            for (int i = issued; i < n_pages; ++i) {
                 if ((i & 31) == 0) {  // next window of page ids; prefetch the one after
                     pid_cur = pid_nxt;
                     pid_nxt = i + 32 + lane < n_pages ? __ldg(bt_cta + i + 32 + lane) : 0;
                 }
                 const int32_t pid = __shfl_sync(0xffffffffu, pid_cur, i & 31);
                 if (!warp_wait(&S.empty[i % kStages], ((i / kStages) & 1) ^ 1, abort, p.err)) break;
-                int ok = 1;
-                if (lane == 0) ok = issue_page(i, pid) ? 1 : 0;
-                if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+                if (lane == 0) issue_page(i, pid);
+                __syncwarp();
                 issued = i + 1;
             }
         }
@@ -1040,8 +974,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
                      : "memory");
     }
-    // No CTA of a cluster leaves while the leader's copies may still target it.
-    if (G > 1) cluster_sync_all();
 }
 
 // ---------------------------------------------------------------- host side
@@ -1083,7 +1015,7 @@ cudaError_t encode_cache_map(CUtensorMap* map, const uint8_t* kv, int64_t num_pa
 }  // namespace
 
 bool tc_supports(const DecodeParams& p, int cc_major, int cc_minor) {
-    return cc_major == 10 && cc_minor == 3 && p.H * p.T <= kMaxClusterRows && p.num_pages >= 1 &&
+    return cc_major == 10 && cc_minor == 3 && p.H * p.T <= kMaxRowsTc && p.num_pages >= 1 &&
            p.num_pages * kPage < (1ll << 31);
 }
 
@@ -1122,22 +1054,10 @@ cudaError_t launch_tc_decode(const DecodeParams& p, cudaStream_t stream, bool* h
     } else if (HT <= kNq) {
         tc_decode_kernel<16><<<dim3(p.n_splits, p.B), kThreads, sizeof(Smem) + 1024, stream>>>(map, p);
     } else {
-        // a cluster of G CTAs (16 rows each) per (split, request)
+        // G CTAs (16 rows each) per (partition, request), adjacent in the grid
         const unsigned G = static_cast<unsigned>((HT + kNq - 1) / kNq);
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(G * static_cast<unsigned>(p.n_splits), static_cast<unsigned>(p.B));
-        cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = sizeof(Smem) + 1024;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = G;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, tc_decode_kernel<16>, map, p);
-        if (e != cudaSuccess) return e;
+        tc_decode_kernel<16><<<dim3(G * static_cast<unsigned>(p.n_splits), static_cast<unsigned>(p.B)), kThreads,
+                               sizeof(Smem) + 1024, stream>>>(map, p);
     }
     e = cudaGetLastError();
     if (e == cudaSuccess) *handled = true;
