@@ -8,8 +8,8 @@
 //
 // Design (GB300-first):
 //   * The FP8 codes are MMA operands as they sit in the cache: every 64-position
-//     page is bulk-copied by one TMA instruction (a 3-D box that lands as nine
-//     64x64-byte tiles with 64-byte swizzle) into a
+//     page is bulk-copied by TMA (one 3-D box, or for the first pages nine 2-D
+//     boxes, landing as nine 64x64-byte tiles with 64-byte swizzle) into a
 //     5-deep shared-memory ring and consumed by tcgen05.mma kind::f8f6f4 with no
 //     dequantisation pass.  kv_scale is folded into the score scale and the
 //     output scale.
@@ -156,7 +156,15 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     return __all_sync(0xffffffffu, wait_bounded(bar, parity, abort, err));
 }
 
-// One whole page (see encode_cache_map): a single copy instruction.
+// One 64 x 64-byte box of a page (see encode_cache_maps).
+__device__ __forceinline__ void tma_load_box(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+// One whole page (see encode_cache_maps): a single copy instruction.
 __device__ __forceinline__ void tma_load_page(uint32_t dst, const CUtensorMap* map, int row, uint64_t* bar) {
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
@@ -343,7 +351,8 @@ __device__ __forceinline__ void split_p(float a0, float a1, uint32_t& c1, uint32
 // operands always use 16-row blocks (rows >= H*T are zero).
 template <int kRows>
 __global__ void __launch_bounds__(kThreads, 1)
-    tc_decode_kernel(const __grid_constant__ CUtensorMap tmap, const DecodeParams p) {
+    tc_decode_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_box,
+                     const DecodeParams p) {
     extern __shared__ uint8_t smem_raw[];
     Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -367,7 +376,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     int32_t pid_cur = 0, pid_nxt = 0;
     uint4 qv[2][3];  // rows warp - 1 and warp + 10, 16-byte chunks lane + 32k
     if (warp == 0) {
-        if (lane == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_box)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
+        }
         pid_cur = pg_begin + lane < p.max_pages ? __ldg(bt_cta + lane) : 0;
         pid_nxt = pg_begin + 32 + lane < p.max_pages ? __ldg(bt_cta + 32 + lane) : 0;
     } else {
@@ -436,7 +448,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the rest of the set-up: issuing a copy can stall its thread for a long
     // time, and the other warps prepare the query and TMEM meanwhile.
     int issued = 0;
-    // Page i into slot i % kStages (one thread).
+    // Page i into slot i % kStages (one thread).  The first kStages pages go
+    // as nine separate boxes, which gets the first bytes in sooner; later pages
+    // as one copy instruction, which keeps the producer's issue cost low.
     auto issue_page = [&](int i, int32_t pid) {
         const int s = i % kStages;
         if (pid < 0 || pid >= p.num_pages) {
@@ -444,7 +458,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             pid = 0;  // load a valid page; the softmax masks and zeroes it
         }
         mbar_expect_tx(&S.full[s], kSlotBytes);
-        tma_load_page(smem_u32(S.slot[s]), &tmap, pid * kPage, &S.full[s]);
+        const uint32_t dst = smem_u32(S.slot[s]);
+        if (i < kStages) {
+#pragma unroll
+            for (int j = 0; j < kBoxes; ++j) tma_load_box(dst + j * kBoxBytes, &tmap_box, 64 * j, pid * kPage, &S.full[s]);
+        } else {
+            tma_load_page(dst, &tmap, pid * kPage, &S.full[s]);
+        }
     };
     if (warp == 0 && n_pages > 0) {
         const int first = min(kStages, n_pages);  // fresh slots: nothing to wait for
@@ -648,22 +668,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool causal = p.T > 1;             // for T = 1 the partition end bounds every row
         const uint32_t to = tmem + (static_cast<uint32_t>(32 * quad) << 16) + kOCol0 + 128 * g;
         const int32_t* bt = p.block_table + (int64_t)b * p.bt_stride + pg_begin;
-        // Per-head values that every lane needs (score scale, reference): with
-        // 12 rows they stay in registers; with 16 they are read from shared
-        // memory as four 16-byte vectors when used, which keeps the 16-row
-        // variant within the register budget.  Each warp keeps its own copy of
-        // the references (identical across the group), so it updates them alone.
+        // Per-head values that every lane needs: the references are read from
+        // shared memory as four 16-byte vectors when used (each warp keeps its
+        // own copy, identical across the group, so it updates them alone); the
+        // score scales stay in registers with 12 rows and come from shared
+        // memory the same way with 16.  This keeps both variants within the
+        // register budget.
         constexpr bool kRegRows = kRows <= 12;
         float lp[kRows];                         // normaliser partials of this thread's positions
         float r_l = NEG;                         // lane h < kRows: reference of head h
-        float r_reg[kRows], rsc_reg[kRows];      // kRegRows only
-        float* rref = S.rref[warp - 4];          // this warp's copy of the references (16 rows)
+        float rsc_reg[kRows];                    // kRegRows only
+        float* rref = S.rref[warp - 4];          // this warp's copy of the references
         if (lane < kNq) rref[lane] = NEG;
         __syncwarp();
 #pragma unroll
         for (int h = 0; h < kRows; ++h) {
             lp[h] = 0.f;
-            r_reg[h] = NEG;
             rsc_reg[h] = kRegRows ? S.row_scale[h] : 0.f;
         }
         bool fail = false;
@@ -691,7 +711,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive(&S.s_empty[sb]);
                 const bool in_part = has_row && page_ok && pos < p_end;
                 float rsc[16];
-                int lim[16];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     if constexpr (kRegRows) {
@@ -701,18 +720,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float4 a4 = reinterpret_cast<const float4*>(S.row_scale)[j];
                         rsc[4 * j] = a4.x, rsc[4 * j + 1] = a4.y, rsc[4 * j + 2] = a4.z, rsc[4 * j + 3] = a4.w;
                     }
-                    if (causal) {
-                        const int4 l4 = reinterpret_cast<const int4*>(S.rowlim)[j];
-                        lim[4 * j] = l4.x, lim[4 * j + 1] = l4.y, lim[4 * j + 2] = l4.z, lim[4 * j + 3] = l4.w;
-                    } else {
-                        lim[4 * j] = lim[4 * j + 1] = lim[4 * j + 2] = lim[4 * j + 3] = 0;
-                    }
                 }
                 float mine = NEG;  // lane h < kRows ends up with this warp's max of head h
 #pragma unroll
                 for (int h = 0; h < kRows; ++h) {
                     const float v = (__uint_as_float(r1[h]) + __uint_as_float(r2[h]) * 0.0625f) * rsc[h];
-                    s[h] = (in_part && (!causal || pos < lim[h])) ? v : NEG;
+                    s[h] = (in_part && (!causal || pos < S.rowlim[h])) ? v : NEG;
                     const float wm = warp_max_redux(s[h]);
                     mine = (lane == h) ? wm : mine;
                 }
@@ -733,15 +746,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float rn = need ? t - kShift : r_l;
                 const float a = need ? exp2f(r_l - rn) : 1.f;  // r_l = -inf: nothing to keep
                 r_l = rn;
-                if constexpr (!kRegRows) {
-                    if (lane < kNq) rref[lane] = rn;
-                    __syncwarp();
-                }
+                if (lane < kNq) rref[lane] = rn;
+                __syncwarp();
                 float al[kRows];
 #pragma unroll
                 for (int h = 0; h < kRows; ++h) {
                     al[h] = __shfl_sync(0xffffffffu, a, h);
-                    if constexpr (kRegRows) r_reg[h] = __shfl_sync(0xffffffffu, rn, h);
                     lp[h] *= al[h];
                 }
                 if (k > 0) {
@@ -772,13 +782,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float r[16];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    if constexpr (kRegRows) {
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) r[4 * j + u] = 4 * j + u < kRows ? r_reg[(4 * j + u) % kRows] : 0.f;
-                    } else {
-                        const float4 a4 = reinterpret_cast<const float4*>(rref)[j];
-                        r[4 * j] = a4.x, r[4 * j + 1] = a4.y, r[4 * j + 2] = a4.z, r[4 * j + 3] = a4.w;
-                    }
+                    const float4 a4 = reinterpret_cast<const float4*>(rref)[j];
+                    r[4 * j] = a4.x, r[4 * j + 1] = a4.y, r[4 * j + 2] = a4.z, r[4 * j + 3] = a4.w;
                 }
 #pragma unroll
                 for (int h = 0; h < kRows; ++h) {
@@ -994,22 +999,39 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
     return fn;
 }
 
-// The cache viewed as a 3-D byte tensor: (64-byte column chunk offset, row =
-// page * 64 + position, chunk of the 576-byte row), strides 576 B (row) and
-// 64 B (chunk).  One box {64, 64, 9} is a whole page, landing in shared memory
-// as nine 64-position x 64-byte tiles (chunk-major) with 64-byte swizzle: the
-// UMMA SWIZZLE_64B K-major layout of each 64-dim slice of the page.
-cudaError_t encode_cache_map(CUtensorMap* map, const uint8_t* kv, int64_t num_pages) {
+// Two views of the cache for the TMA unit.
+//  * 3-D byte tensor (64-byte column offset, row = page * 64 + position, 64-byte
+//    chunk of the 576-byte row), strides 576 B (row) and 64 B (chunk): one box
+//    {64, 64, 9} is a whole page, landing in shared memory as nine 64-position x
+//    64-byte tiles (chunk-major) with 64-byte swizzle -- the UMMA SWIZZLE_64B
+//    K-major layout of each 64-dim slice of the page.
+//  * 2-D byte tensor [rows][576] with 64 x 64-byte boxes and the same swizzle:
+//    the same nine tiles as nine copies.
+cudaError_t encode_cache_maps(CUtensorMap* map3, CUtensorMap* map2, const uint8_t* kv, int64_t num_pages) {
     auto fn = get_encode_fn();
     if (!fn) return cudaErrorNotSupported;
-    cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(num_pages * kPage), static_cast<cuuint64_t>(kBoxes)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(kDqk), 64};
-    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kPage), static_cast<cuuint32_t>(kBoxes)};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(kv), dims, strides, box,
-                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+    const cuuint64_t rows = static_cast<cuuint64_t>(num_pages * kPage);
+    {
+        cuuint64_t dims[3] = {64, rows, static_cast<cuuint64_t>(kBoxes)};
+        cuuint64_t strides[2] = {static_cast<cuuint64_t>(kDqk), 64};
+        cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kPage), static_cast<cuuint32_t>(kBoxes)};
+        cuuint32_t estr[3] = {1, 1, 1};
+        CUresult r = fn(map3, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(kv), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    {
+        cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDqk), rows};
+        cuuint64_t strides[1] = {static_cast<cuuint64_t>(kDqk)};
+        cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kPage)};
+        cuuint32_t estr[2] = {1, 1};
+        CUresult r = fn(map2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(kv), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace
@@ -1046,18 +1068,18 @@ cudaError_t launch_tc_decode(const DecodeParams& p, cudaStream_t stream, bool* h
     }
     if (!tc_supports(p, cc[dev][0], cc[dev][1])) return cudaSuccess;
 
-    CUtensorMap map;
-    if ((e = encode_cache_map(&map, p.kv, p.num_pages)) != cudaSuccess) return e;
+    CUtensorMap map, map_box;
+    if ((e = encode_cache_maps(&map, &map_box, p.kv, p.num_pages)) != cudaSuccess) return e;
     const int HT = p.H * p.T;
     if (HT <= 12) {
-        tc_decode_kernel<12><<<dim3(p.n_splits, p.B), kThreads, sizeof(Smem) + 1024, stream>>>(map, p);
+        tc_decode_kernel<12><<<dim3(p.n_splits, p.B), kThreads, sizeof(Smem) + 1024, stream>>>(map, map_box, p);
     } else if (HT <= kNq) {
-        tc_decode_kernel<16><<<dim3(p.n_splits, p.B), kThreads, sizeof(Smem) + 1024, stream>>>(map, p);
+        tc_decode_kernel<16><<<dim3(p.n_splits, p.B), kThreads, sizeof(Smem) + 1024, stream>>>(map, map_box, p);
     } else {
         // G CTAs (16 rows each) per (partition, request), adjacent in the grid
         const unsigned G = static_cast<unsigned>((HT + kNq - 1) / kNq);
         tc_decode_kernel<16><<<dim3(G * static_cast<unsigned>(p.n_splits), static_cast<unsigned>(p.B)), kThreads,
-                               sizeof(Smem) + 1024, stream>>>(map, p);
+                               sizeof(Smem) + 1024, stream>>>(map, map_box, p);
     }
     e = cudaGetLastError();
     if (e == cudaSuccess) *handled = true;
