@@ -33,8 +33,14 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Launched as a programmatic dependent of the decode kernel (pdl): wait for
+// its partials, and let the next kernel's CTAs be scheduled meanwhile (the
+// decode kernel waits for this one before reading anything).
 __device__ __forceinline__ void wait_for_producer(int pdl) {
-    if (pdl) asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (pdl) {
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+    }
 }
 
 template <bool kBf16In>

@@ -357,6 +357,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int HT = p.H * p.T;
+    // Launched as a programmatic dependent of the previous kernel on the stream:
+    // everything before this point overlaps its tail; nothing is read before it.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // More than 16 rows: G = ceil(H*T / 16) CTAs per (partition, request), CTA
     // r taking rows [16r, 16r + 16) of every page.  They are adjacent in the
     // grid, so they run at the same time and all but the first read each page
@@ -1071,16 +1074,24 @@ cudaError_t launch_tc_decode(const DecodeParams& p, cudaStream_t stream, bool* h
     CUtensorMap map, map_box;
     if ((e = encode_cache_maps(&map, &map_box, p.kv, p.num_pages)) != cudaSuccess) return e;
     const int HT = p.H * p.T;
-    if (HT <= 12) {
-        tc_decode_kernel<12><<<dim3(p.n_splits, p.B), kThreads, sizeof(Smem) + 1024, stream>>>(map, map_box, p);
-    } else if (HT <= kNq) {
-        tc_decode_kernel<16><<<dim3(p.n_splits, p.B), kThreads, sizeof(Smem) + 1024, stream>>>(map, map_box, p);
-    } else {
-        // G CTAs (16 rows each) per (partition, request), adjacent in the grid
-        const unsigned G = static_cast<unsigned>((HT + kNq - 1) / kNq);
-        tc_decode_kernel<16><<<dim3(G * static_cast<unsigned>(p.n_splits), static_cast<unsigned>(p.B)), kThreads,
-                               sizeof(Smem) + 1024, stream>>>(map, map_box, p);
-    }
+    // G CTAs (16 rows each) per (partition, request), adjacent in the grid
+    const unsigned G = HT <= kNq ? 1u : static_cast<unsigned>((HT + kNq - 1) / kNq);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(G * static_cast<unsigned>(p.n_splits), static_cast<unsigned>(p.B));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = sizeof(Smem) + 1024;
+    cfg.stream = stream;
+    // Programmatic dependent launch: the CTAs may be scheduled while the
+    // previous kernel on the stream drains; the kernel waits for it
+    // (griddepcontrol.wait) before reading anything.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = HT <= 12 ? cudaLaunchKernelEx(&cfg, tc_decode_kernel<12>, map, map_box, p)
+                 : cudaLaunchKernelEx(&cfg, tc_decode_kernel<16>, map, map_box, p);
+    if (e != cudaSuccess) return e;
     e = cudaGetLastError();
     if (e == cudaSuccess) *handled = true;
     return e;
