@@ -86,9 +86,7 @@ struct Smem {
     uint64_t s_full[kSBufs], s_empty[kSBufs];
     uint64_t p_full[kGroups][2];             // group's probabilities of its page are ready
     uint64_t pv_done[kGroups][2];            // group's PV of its page k done (buffer k & 1)
-    uint64_t red_bar[kGroups][2];
     uint64_t fin_l_bar[kGroups];             // group's normaliser partials are written
-    uint64_t fin_bar;                        // groups 1.. parked their final state
     uint64_t mma_done[3];                    // per MMA-issuing thread: its MMAs drained
     uint32_t tmem_base;
     int abort;
@@ -437,10 +435,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 2; ++i) {
                 mbar_init(&S.pv_done[g][i], 1);
                 mbar_init(&S.p_full[g][i], 4);
-                mbar_init(&S.red_bar[g][i], 4);
             }
         }
-        mbar_init(&S.fin_bar, 4 * (kGroups - 1));
         for (int i = 0; i < 3; ++i) mbar_init(&S.mma_done[i], 1);
         S.abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -861,99 +857,95 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 
         // ---- merge the warpgroups' running states; write the answer ----
-        // Warpgroup 1 parks its tile as [row][512] fp32 in a page slot that no
-        // copy or MMA touches any more (the slot of its own last page, or an
-        // unused one); warpgroup 0 merges it with its own tile, still in
-        // registers, stages the answer rows in the next slot and sends them in
-        // one bulk copy (they are contiguous in global memory).
+        // Both warpgroups park their tiles as [row][512] fp32 in page slots that
+        // no copy or MMA touches any more (warpgroup 1: the slot of its own last
+        // page, or an unused one; warpgroup 0: the next slot).  Each then merges
+        // half of the rows in place into warpgroup 0's tile, and the answer rows
+        // leave in one bulk copy (they are contiguous in global memory).  The
+        // eight warps meet at named barrier 4, each exactly three times.
         static_assert(kGroups == 2, "the staging slots assume two warpgroups");
         const int sl_park = [&] {
             const int c1 = n_pages > 1 ? (n_pages - 1 + kGroups - 1) / kGroups : 0;
             return c1 > 0 ? (1 + kGroups * (c1 - 1)) % kStages : kStages - 1;
         }();
-        float* park = reinterpret_cast<float*>(S.slot[sl_park]);
-        float* stage = reinterpret_cast<float*>(S.slot[(sl_park + 1) % kStages]);
+        float* tile1 = reinterpret_cast<float*>(S.slot[sl_park]);
+        float* tile0 = reinterpret_cast<float*>(S.slot[(sl_park + 1) % kStages]);
         __nv_bfloat16* stage_bf = reinterpret_cast<__nv_bfloat16*>(S.slot[(sl_park + 2) % kStages]);
-        if (g > 0) {
+        {
+            float* mine = g == 0 ? tile0 : tile1;
 #pragma unroll
             for (int c = 0; c < 4; ++c)
 #pragma unroll
-                for (int h = 0; h < kRows; ++h) park[h * kDv + 128 * c + d] = o[c][h];
+                for (int h = 0; h < kRows; ++h) mine[h * kDv + 128 * c + d] = o[c][h];
             if (quad == 0 && lane < kNq) {
                 S.fin[g][0][lane] = m_run;
                 S.fin[g][1][lane] = l_run;
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&S.fin_bar);
-        } else {
-            const bool ok = __all_sync(0xffffffffu, wait_bounded(&S.fin_bar, 0, abort, p.err));
-            const bool direct = p.n_splits == 1;
+        }
+        asm volatile("bar.sync 4, 256;" ::: "memory");  // both tiles and states parked
+        const bool direct = p.n_splits == 1;
+        if (g == 0 && quad == 0 && lane < kNq) {
             // lane h: the weight of each tile (normaliser and kv_scale folded in)
-            if (quad == 0 && lane < kNq) {
-                float mn = m_run, l = l_run, w0 = 1.f, w1 = 0.f;
-                if (ok) {
-                    const float m1 = S.fin[1][0][lane], l1 = S.fin[1][1][lane];
-                    mn = fmaxf(m_run, m1);
-                    if (mn != NEG) {
-                        w0 = exp2f(m_run - mn);
-                        w1 = exp2f(m1 - mn);
-                        l = l_run * w0 + l1 * w1;
-                    }
-                }
-                const float inv = (l > 0.f) ? kv_scale / l : 0.f;
-                S.wrow[0][lane] = w0 * inv;
-                S.wrow[1][lane] = w1 * inv;
-                if (lane < HTc) {
-                    const float lse = (l > 0.f) ? (mn + log2f(l)) * kLn2 : -INFINITY;
-                    const int64_t grow = (int64_t)b * HT + r0 + lane;
-                    if (direct) {
-                        if (p.lse) p.lse[grow] = lse;
-                    } else {
-                        p.part_lse[(int64_t)split * p.B * HT + grow] = lse;
-                    }
+            const float m0 = S.fin[0][0][lane], l0 = S.fin[0][1][lane];
+            const float m1 = S.fin[1][0][lane], l1 = S.fin[1][1][lane];
+            const float mn = fmaxf(m0, m1);
+            float w0 = 0.f, w1 = 0.f, l = 0.f;
+            if (mn != NEG) {
+                w0 = exp2f(m0 - mn);
+                w1 = exp2f(m1 - mn);
+                l = l0 * w0 + l1 * w1;
+            }
+            const float inv = (l > 0.f) ? kv_scale / l : 0.f;
+            S.wrow[0][lane] = w0 * inv;
+            S.wrow[1][lane] = w1 * inv;
+            if (lane < HTc) {
+                const float lse = (l > 0.f) ? (mn + log2f(l)) * kLn2 : -INFINITY;
+                const int64_t grow = (int64_t)b * HT + r0 + lane;
+                if (direct) {
+                    if (p.lse) p.lse[grow] = lse;
+                } else {
+                    p.part_lse[(int64_t)split * p.B * HT + grow] = lse;
                 }
             }
-            asm volatile("bar.sync 1, 128;" ::: "memory");  // warpgroup 0: weights
+        }
+        asm volatile("bar.sync 4, 256;" ::: "memory");  // weights
+        {
+            // Rows [g * kHalf, g * kHalf + kHalf) of this warpgroup: every load first.
+            constexpr int kHalf = (kRows + 1) / 2;
+            float w0[kHalf], w1[kHalf], t0[kHalf][4], t1[kHalf][4];
+#pragma unroll
+            for (int j = 0; j < kHalf; ++j) {
+                const int h = g * kHalf + j;
+                w0[j] = S.wrow[0][h < kNq ? h : 0];
+                w1[j] = S.wrow[1][h < kNq ? h : 0];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    t0[j][c] = h < HTc ? tile0[h * kDv + 128 * c + d] : 0.f;
+                    t1[j][c] = h < HTc ? tile1[h * kDv + 128 * c + d] : 0.f;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kHalf; ++j) {
+                const int h = g * kHalf + j;
+                if (h >= HTc) break;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float v = fmaf(t1[j][c], w1[j], t0[j][c] * w0[j]);
+                    if (direct)
+                        stage_bf[h * kDv + 128 * c + d] = __float2bfloat16_rn(v);
+                    else
+                        tile0[h * kDv + 128 * c + d] = v;
+                }
+            }
+        }
+        fence_async_smem();  // staged rows: generic writes -> bulk-copy reads
+        asm volatile("bar.sync 4, 256;" ::: "memory");  // answer rows staged
+        if (g == 0) {
             const int n = HTc * kDv;
-            // Every load first (the parked tile and the weights), then the
-            // products and the staging stores.
-            float w0[kRows], w1[kRows];
-#pragma unroll
-            for (int h = 0; h < kRows; ++h) {
-                w0[h] = S.wrow[0][h];
-                w1[h] = S.wrow[1][h];
-            }
-            // All loads of a round first: the whole parked tile with 12 rows, one
-            // 128-dim block at a time with 16 (register budget).
-            constexpr int kRounds = kRows <= 12 ? 1 : 4;
-#pragma unroll
-            for (int c0 = 0; c0 < 4; c0 += 4 / kRounds) {
-                float pk[4 / kRounds][kRows];
-#pragma unroll
-                for (int cc = 0; cc < 4 / kRounds; ++cc)
-#pragma unroll
-                    for (int h = 0; h < kRows; ++h)
-                        pk[cc][h] = (ok && h < HTc) ? park[h * kDv + 128 * (c0 + cc) + d] : 0.f;
-#pragma unroll
-                for (int cc = 0; cc < 4 / kRounds; ++cc) {
-                    const int c = c0 + cc;
-#pragma unroll
-                    for (int h = 0; h < kRows; ++h) {
-                        if (h >= HTc) break;
-                        const float v = fmaf(pk[cc][h], w1[h], o[c][h] * w0[h]);
-                        if (direct)
-                            stage_bf[h * kDv + 128 * c + d] = __float2bfloat16_rn(v);
-                        else
-                            stage[h * kDv + 128 * c + d] = v;
-                    }
-                }
-            }
-            fence_async_smem();  // staged rows: generic writes -> bulk-copy reads
-            asm volatile("bar.sync 1, 128;" ::: "memory");
             const int64_t row0 = (int64_t)b * HT + r0;  // this CTA's first answer row
             void* dst = direct ? static_cast<void*>(p.out + row0 * kDv)
                                : static_cast<void*>(p.part_out + ((int64_t)split * p.B * HT + row0) * kDv);
-            const void* src = direct ? static_cast<const void*>(stage_bf) : static_cast<const void*>(stage);
+            const void* src = direct ? static_cast<const void*>(stage_bf) : static_cast<const void*>(tile0);
             const uint32_t bytes = static_cast<uint32_t>(n) * (direct ? 2u : 4u);
             if ((reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
                 if (tid == 128 && bytes > 0) {
@@ -962,14 +954,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  "r"(smem_u32(src)), "r"(bytes)
                                  : "memory");
                     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-                    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+                    // Only the shared-memory reads must finish before the CTA
+                    // leaves; the writes complete with the grid.
+                    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
                 }
             } else {  // destination not 16-byte aligned: plain stores
                 for (int idx = tid - 128; idx < n; idx += 128) {
                     if (direct)
                         static_cast<__nv_bfloat16*>(dst)[idx] = stage_bf[idx];
                     else
-                        static_cast<float*>(dst)[idx] = stage[idx];
+                        static_cast<float*>(dst)[idx] = tile0[idx];
                 }
             }
         }
