@@ -27,7 +27,7 @@ _DTYPES = {torch.bfloat16: 1, torch.float32: 2, torch.uint8: 3, torch.float8_e4m
 EXPORTS = ("mla_decode_paged", "mla_merge_partials", "mla_auto_splits", "mla_split_chunk_pages",
            "mla_decode_workspace_bytes", "mla_set_impl", "mla_device_error", "mla_status_string",
            "mla_last_error", "mla_profile_next_decode", "mla_last_decode_impl",
-           "mla_decode_paged_noalloc")
+           "mla_decode_paged_noalloc", "mla_test_stall_copies")
 
 
 class MlaError(RuntimeError):
@@ -61,6 +61,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mla_decode_workspace_bytes.restype = ctypes.c_size_t
     lib.mla_set_impl.argtypes = [ctypes.c_int32]
     lib.mla_set_impl.restype = ctypes.c_int32
+    lib.mla_test_stall_copies.argtypes = [ctypes.c_int]
+    lib.mla_test_stall_copies.restype = ctypes.c_int
     lib.mla_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32), P]
     lib.mla_device_error.restype = ctypes.c_int
     lib.mla_last_decode_impl.argtypes = []
@@ -158,6 +160,13 @@ def mla_decode_workspace_bytes(B, T, H, n_splits):
 
 def mla_set_impl(impl: int) -> int:
     return lib().mla_set_impl(impl)
+
+
+def mla_test_stall_copies(on: bool) -> int:
+    """Failure-detection tests only: later tensor-core launches issue no page
+    copies, so their bounded waits run out (device error 1).  Returns the
+    previous setting."""
+    return lib().mla_test_stall_copies(1 if on else 0)
 
 
 def mla_last_decode_impl() -> int:

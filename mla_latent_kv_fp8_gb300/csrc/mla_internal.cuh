@@ -43,6 +43,7 @@ struct DecodeParams {
     float* part_out;
     float* part_lse;
     int* err;                   // device error word
+    int test_stall_copies;      // failure-detection tests only: issue no page copies
 };
 
 struct MergeParams {

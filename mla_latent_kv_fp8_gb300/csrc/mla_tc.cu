@@ -42,6 +42,7 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "mla_internal.cuh"
@@ -465,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_page(dst, &tmap, pid * kPage, &S.full[s]);
         }
     };
-    if (warp == 0 && n_pages > 0) {
+    if (warp == 0 && n_pages > 0 && !p.test_stall_copies) {
         const int first = min(kStages, n_pages);  // fresh slots: nothing to wait for
         for (int i = 0; i < first; ++i) {
             const int32_t pid = __shfl_sync(0xffffffffu, pid_cur, i);
@@ -546,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ======================= TMA producer =======================
-        if (n_pages > 0) {
+        if (n_pages > 0 && !p.test_stall_copies) {
             for (int i = issued; i < n_pages; ++i) {
                 if ((i & 31) == 0) {  // next window of page ids; prefetch the one after
                     pid_cur = pid_nxt;
@@ -1033,6 +1034,10 @@ cudaError_t encode_cache_maps(CUtensorMap* map3, CUtensorMap* map2, const uint8_
 
 }  // namespace
 
+// Failure-detection tests only (mla_test_stall_copies): launches issue no page
+// copies, so every wait for a page runs out.
+std::atomic<int> g_test_stall_copies{0};
+
 bool tc_supports(const DecodeParams& p, int cc_major, int cc_minor) {
     return cc_major == 10 && cc_minor == 3 && p.H * p.T <= kMaxRowsTc && p.num_pages >= 1 &&
            p.num_pages * kPage < (1ll << 31);
@@ -1083,8 +1088,10 @@ cudaError_t launch_tc_decode(const DecodeParams& p, cudaStream_t stream, bool* h
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = HT <= 12 ? cudaLaunchKernelEx(&cfg, tc_decode_kernel<12>, map, map_box, p)
-                 : cudaLaunchKernelEx(&cfg, tc_decode_kernel<16>, map, map_box, p);
+    DecodeParams q = p;
+    q.test_stall_copies = g_test_stall_copies.load();
+    e = HT <= 12 ? cudaLaunchKernelEx(&cfg, tc_decode_kernel<12>, map, map_box, q)
+                 : cudaLaunchKernelEx(&cfg, tc_decode_kernel<16>, map, map_box, q);
     if (e != cudaSuccess) return e;
     e = cudaGetLastError();
     if (e == cudaSuccess) *handled = true;
@@ -1092,3 +1099,7 @@ cudaError_t launch_tc_decode(const DecodeParams& p, cudaStream_t stream, bool* h
 }
 
 }  // namespace mla
+
+extern "C" int mla_test_stall_copies(int on) {
+    return mla::g_test_stall_copies.exchange(on ? 1 : 0);
+}
