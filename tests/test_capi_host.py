@@ -60,6 +60,20 @@ def test_auto_splits(L, B, max_pages, sm, expect):
     assert -(-max_pages // chunk) == s  # every partition non-empty at full length
 
 
+@pytest.mark.parametrize("B,T,H,max_pages,sm,expect", [
+    (32, 1, 96, 278, 152, 3),      # 96 rows: 6 CTAs per unit, wave cost model
+    (16, 4, 12, 1568, 152, 10),    # 48 rows over mixed lengths: the 160-page cap
+    (128, 1, 12, 2219, 152, 14),   # many requests of mixed length: the 160-page cap
+    (8, 1, 12, 512, 152, 19),      # one wave, as before
+])
+def test_auto_splits_rows_and_cap(L, B, T, H, max_pages, sm, expect):
+    s = L.mla_auto_splits(B, T, H, max_pages, sm)
+    assert s == expect
+    chunk = L.mla_split_chunk_pages(max_pages, s)
+    assert chunk <= 160 and chunk % 2 == 0
+    assert -(-max_pages // chunk) == s
+
+
 def test_workspace_bytes(L):
     assert L.mla_decode_workspace_bytes(8, 1, 12, 1) == 0
     n = L.mla_decode_workspace_bytes(8, 1, 12, 19)
