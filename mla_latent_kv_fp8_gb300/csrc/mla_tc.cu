@@ -82,7 +82,6 @@ struct Smem {
     float wrow[kGroups][kNq];                // final weight of each group's tile, by head
     alignas(16) float row_scale[kNq];        // kv_scale * sm_scale * log2(e) * 2^-e
     alignas(16) int rowlim[kNq];             // visible prefix per row; -1 = padding
-    alignas(16) float rref[4 * kGroups][kNq];  // per attention warp: reference of each head
     uint64_t full[kStages], empty[kStages];
     uint64_t s_full[kSBufs], s_empty[kSBufs];
     uint64_t p_full[kGroups][2];             // group's probabilities of its page are ready
@@ -124,6 +123,16 @@ __device__ __forceinline__ float warp_max_redux(float v) {
     float r;
     asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
     return r;
+}
+// Max over each 16-lane half of the warp (the halves reduce independently).
+// Four xor shuffles: a redux.sync whose member mask differs between the two
+// halves measured several times slower.
+__device__ __forceinline__ float half_warp_max(float v) {
+    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+    return v;
 }
 __device__ __forceinline__ uint64_t global_ns() {
     uint64_t t;
@@ -661,30 +670,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         // mbarrier wait.
         const int g = (warp - 4) >> 2;
         const int quad = warp & 3;               // TMEM lane quadrant of this warp
-        const bool has_row = lane < 16;          // M=64 score tile: 16 rows per quadrant
-        const int pr = 16 * quad + lane;         // position within the page
+        // The M=64 score tile holds 16 positions per TMEM lane quadrant (lanes
+        // 0..15).  Lane l < 16 keeps heads 0..7 of position l, and lane l + 16
+        // receives heads 8..15 of the same position: every lane of the warp
+        // works on 8 heads of one position.
+        const int half = lane >> 4;              // 0: heads 0..7, 1: heads 8..15
+        const int pr = 16 * quad + (lane & 15);  // position within the page
         const int d = 32 * quad + lane;          // latent dim within each 128-dim block
         const float NEG = -INFINITY;
         const bool causal = p.T > 1;             // for T = 1 the partition end bounds every row
         const uint32_t to = tmem + (static_cast<uint32_t>(32 * quad) << 16) + kOCol0 + 128 * g;
         const int32_t* bt = p.block_table + (int64_t)b * p.bt_stride + pg_begin;
-        // Per-head values that every lane needs: the references are read from
-        // shared memory as four 16-byte vectors when used (each warp keeps its
-        // own copy, identical across the group, so it updates them alone); the
-        // score scales stay in registers with 12 rows and come from shared
-        // memory the same way with 16.  This keeps both variants within the
-        // register budget.
-        constexpr bool kRegRows = kRows <= 12;
-        float lp[kRows];                         // normaliser partials of this thread's positions
+        // Per lane, for its 8 heads h = 8 * half + j: normaliser partial, score
+        // scale and reference (heads >= kRows are padding).
+        constexpr int kHL = 8;
+        float lp[kHL], rsc[kHL], rr[kHL];
         float r_l = NEG;                         // lane h < kRows: reference of head h
-        float rsc_reg[kRows];                    // kRegRows only
-        float* rref = S.rref[warp - 4];          // this warp's copy of the references
-        if (lane < kNq) rref[lane] = NEG;
-        __syncwarp();
 #pragma unroll
-        for (int h = 0; h < kRows; ++h) {
-            lp[h] = 0.f;
-            rsc_reg[h] = kRegRows ? S.row_scale[h] : 0.f;
+        for (int j = 0; j < kHL; ++j) {
+            const int h = kHL * half + j;
+            lp[j] = 0.f;
+            rr[j] = NEG;
+            rsc[j] = h < kRows ? S.row_scale[h] : 0.f;
         }
         bool fail = false;
         int k = 0;
@@ -696,7 +703,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (i + kGroups < n_pages) pid_next = __ldg(bt + i + kGroups);
             const bool page_ok = pid >= 0 && pid < p.num_pages;
             const int pos = (pg_begin + i) * kPage + pr;
-            float s[kRows];
+            float s[kHL];
             // ---- scores of this page; this warp's maximum of each head ----
             if (!fail) fail = !warp_wait(&S.s_full[sb], (i / kSBufs) & 1, abort, p.err);
             if (!fail) {
@@ -709,27 +716,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&S.s_empty[sb]);
-                const bool in_part = has_row && page_ok && pos < p_end;
-                float rsc[16];
+                const bool in_part = page_ok && pos < p_end;
+                float mine = NEG;  // lanes 8*half + j (j < 8): this warp's max of head 8*half + j
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    if constexpr (kRegRows) {
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) rsc[4 * j + u] = 4 * j + u < kRows ? rsc_reg[(4 * j + u) % kRows] : 0.f;
-                    } else {
-                        const float4 a4 = reinterpret_cast<const float4*>(S.row_scale)[j];
-                        rsc[4 * j] = a4.x, rsc[4 * j + 1] = a4.y, rsc[4 * j + 2] = a4.z, rsc[4 * j + 3] = a4.w;
-                    }
+                for (int j = 0; j < kHL; ++j) {
+                    const int h = kHL * half + j;
+                    // S1 + S2/16 of heads j (kept) and 8 + j (sent to lane + 16)
+                    const float lo = __uint_as_float(r1[j]) + __uint_as_float(r2[j]) * 0.0625f;
+                    const float hi = __uint_as_float(r1[8 + j]) + __uint_as_float(r2[8 + j]) * 0.0625f;
+                    const float moved = __shfl_xor_sync(0xffffffffu, hi, 16);
+                    const float v = (half ? moved : lo) * rsc[j];
+                    s[j] = (h < kRows && in_part && (!causal || pos < S.rowlim[h])) ? v : NEG;
+                    const float wm = half_warp_max(s[j]);
+                    mine = ((lane & 15) == j) ? wm : mine;
                 }
-                float mine = NEG;  // lane h < kRows ends up with this warp's max of head h
-#pragma unroll
-                for (int h = 0; h < kRows; ++h) {
-                    const float v = (__uint_as_float(r1[h]) + __uint_as_float(r2[h]) * 0.0625f) * rsc[h];
-                    s[h] = (in_part && (!causal || pos < S.rowlim[h])) ? v : NEG;
-                    const float wm = warp_max_redux(s[h]);
-                    mine = (lane == h) ? wm : mine;
-                }
-                if (lane < kNq) S.red_m[g][kb][lane][quad] = mine;  // rows >= kRows: -inf
+                if ((lane & 15) < kHL) S.red_m[g][kb][kHL * half + (lane & 15)][quad] = mine;  // rows >= kRows: -inf
             }
             if (group_sync_or(g, fail)) {
                 fail = true;
@@ -746,14 +747,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float rn = need ? t - kShift : r_l;
                 const float a = need ? exp2f(r_l - rn) : 1.f;  // r_l = -inf: nothing to keep
                 r_l = rn;
-                if (lane < kNq) rref[lane] = rn;
-                __syncwarp();
-                float al[kRows];
 #pragma unroll
-                for (int h = 0; h < kRows; ++h) {
-                    al[h] = __shfl_sync(0xffffffffu, a, h);
-                    lp[h] *= al[h];
+                for (int j = 0; j < kHL; ++j) {
+                    rr[j] = __shfl_sync(0xffffffffu, rn, kHL * half + j);
+                    lp[j] *= __shfl_sync(0xffffffffu, a, kHL * half + j);
                 }
+
                 if (k > 0) {
                     // The tile holds PV of this group's pages 0..k-1: wait for the
                     // last of them, then scale every head's columns.
@@ -767,8 +766,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tmem_ld32(to + 32 * c, v);
                             tmem_wait_ld();
 #pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                if ((j & 15) < kRows) v[j] = __float_as_uint(__uint_as_float(v[j]) * al[j & 15]);
+                            for (int j = 0; j < 32; ++j) {
+                                const float al = __shfl_sync(0xffffffffu, a, j & 15);  // lane h: head h
+                                if ((j & 15) < kRows) v[j] = __float_as_uint(__uint_as_float(v[j]) * al);
+                            }
                             tmem_st32(to + 32 * c, v);
                         }
                         tmem_wait_st();
@@ -779,33 +780,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Buffer kb was last read by this group's PV two pages ago.
             if (!fail && k >= 2) fail = !warp_wait(&S.pv_done[g][kb], ((k >> 1) - 1) & 1, abort, p.err);
             if (!fail) {
-                float r[16];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float4 a4 = reinterpret_cast<const float4*>(rref)[j];
-                    r[4 * j] = a4.x, r[4 * j + 1] = a4.y, r[4 * j + 2] = a4.z, r[4 * j + 3] = a4.w;
+                for (int j = 0; j < kHL; ++j) {
+                    s[j] = (s[j] == NEG) ? 0.f : exp2f(s[j] - rr[j]);
+                    lp[j] += s[j];
                 }
+                {
+                    // 8 bytes of p1 codes and 8 of p2 codes: heads 8*half .. 8*half + 7
+                    uint32_t w1[2] = {0, 0}, w2[2] = {0, 0};
 #pragma unroll
-                for (int h = 0; h < kRows; ++h) {
-                    s[h] = (s[h] == NEG) ? 0.f : exp2f(s[h] - r[h]);
-                    lp[h] += s[h];
-                }
-                if (has_row) {
-                    uint32_t w1[4] = {0, 0, 0, 0}, w2[4] = {0, 0, 0, 0};
-#pragma unroll
-                    for (int h = 0; h < kRows; h += 2) {
+                    for (int j = 0; j < kHL; j += 2) {
                         uint32_t c1, c2;
-                        split_p(s[h], s[h + 1], c1, c2);
-                        w1[h >> 2] |= (c1 & 0xffffu) << (8 * (h & 3));
-                        w2[h >> 2] |= (c2 & 0xffffu) << (8 * (h & 3));
+                        split_p(s[j], s[j + 1], c1, c2);
+                        w1[j >> 2] |= (c1 & 0xffffu) << (8 * (j & 3));
+                        w2[j >> 2] |= (c2 & 0xffffu) << (8 * (j & 3));
                     }
                     uint8_t* pp = S.pp[g][kb];
-                    *reinterpret_cast<uint4*>(pp + pp_off(0, pr)) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
-                    *reinterpret_cast<uint4*>(pp + pp_off(kNq, pr)) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
+                    *reinterpret_cast<uint2*>(pp + pp_off(kHL * half, pr)) = make_uint2(w1[0], w1[1]);
+                    *reinterpret_cast<uint2*>(pp + pp_off(kNq + kHL * half, pr)) = make_uint2(w2[0], w2[1]);
                     // Rows past the partition's end (or of a page whose id was out of
                     // range) may hold anything, even NaN codes: zero them so that
                     // 0 * x stays 0 in the PV product.
-                    if (!page_ok || pos >= p_end) {
+                    if (half == 0 && (!page_ok || pos >= p_end)) {
                         uint8_t* row = S.slot[i % kStages] + pr * 64;
 #pragma unroll
                         for (int j = 0; j < kBoxes; ++j) {
@@ -844,7 +840,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
             float e[kNq];
 #pragma unroll
-            for (int h = 0; h < kNq; ++h) e[h] = h < kRows ? lp[h] : 0.f;
+            for (int h = 0; h < kNq; ++h) e[h] = (h < kRows && (h >> 3) == half) ? lp[h & 7] : 0.f;
             const float wsum = warp_transpose_reduce<false>(e, lane);
             if ((lane & 1) == 0) S.red_l[g][lane >> 1][quad] = wsum;
             __syncwarp();
