@@ -124,16 +124,6 @@ __device__ __forceinline__ float warp_max_redux(float v) {
     asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
     return r;
 }
-// Max over each 16-lane half of the warp (the halves reduce independently).
-// Four xor shuffles: a redux.sync whose member mask differs between the two
-// halves measured several times slower.
-__device__ __forceinline__ float half_warp_max(float v) {
-    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
-    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
-    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
-    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
-    return v;
-}
 __device__ __forceinline__ uint64_t global_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -727,8 +717,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float moved = __shfl_xor_sync(0xffffffffu, hi, 16);
                     const float v = (half ? moved : lo) * rsc[j];
                     s[j] = (h < kRows && in_part && (!causal || pos < S.rowlim[h])) ? v : NEG;
-                    const float wm = half_warp_max(s[j]);
-                    mine = ((lane & 15) == j) ? wm : mine;
+                    // head j of half 0 and head 8 + j of half 1: one full-warp
+                    // reduction each, the other half contributing -inf
+                    const float wlo = warp_max_redux(half ? NEG : s[j]);
+                    const float whi = warp_max_redux(half ? s[j] : NEG);
+                    mine = ((lane & 15) == j) ? (half ? whi : wlo) : mine;
                 }
                 if ((lane & 15) < kHL) S.red_m[g][kb][kHL * half + (lane & 15)][quad] = mine;  // rows >= kRows: -inf
             }
