@@ -175,8 +175,9 @@ mla_status_t mla_decode_paged_noalloc(const mla_tensor_t *q, const mla_tensor_t 
  * Pure host function; sm_count <= 0 means "query the current device". */
 int32_t mla_auto_splits(int32_t B, int32_t T, int32_t H, int32_t max_pages, int32_t sm_count);
 
-/* Pages per partition for a given split count (even, so partitions are whole
- * 128-position tiles), and the number of non-empty partitions per request. */
+/* Pages per partition for a given split count: ceil(max_pages / n_splits),
+ * so that the partitions of a full-length request differ by at most one
+ * page, except the last, which takes the remainder. */
 int32_t mla_split_chunk_pages(int32_t max_pages, int32_t n_splits);
 
 /* Bytes of library scratch one mla_decode_paged call with these sizes uses

@@ -219,17 +219,16 @@ int32_t mla_auto_splits(int32_t B, int32_t T, int32_t H, int32_t max_pages, int3
     if (s < ceil_div(max_pages, kChunkCapPages)) s = ceil_div(max_pages, kChunkCapPages);
     if (s > most) s = most;
     if (s < 1) s = 1;
-    // Snap to the count that equal even-page chunks actually produce.
+    // Snap to the count that equal chunks actually produce.
     const int64_t chunk = mla_split_chunk_pages(max_pages, (int32_t)s);
     return (int32_t)ceil_div(max_pages, chunk);
 }
 
 int32_t mla_split_chunk_pages(int32_t max_pages, int32_t n_splits) {
-    if (max_pages <= 0) return 2;
+    if (max_pages <= 0) return 1;
     if (n_splits < 1) n_splits = 1;
-    int64_t chunk = ceil_div(max_pages, n_splits);
-    chunk += chunk & 1;
-    return (int32_t)(chunk < 2 ? 2 : chunk);
+    const int64_t chunk = ceil_div(max_pages, n_splits);
+    return (int32_t)(chunk < 1 ? 1 : chunk);
 }
 
 size_t mla_decode_workspace_bytes(int32_t B, int32_t T, int32_t H, int32_t n_splits) {
