@@ -10,6 +10,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import struct
 
 import torch
 
@@ -46,6 +47,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         raise ImportError(f"{path} is missing: build it with `python -c \"import __graft_entry__ as g; "
                           f"g.build()\"` (nvcc, sm_103a)")
     lib = ctypes.CDLL(path)
+    if ctypes.sizeof(mla_tensor_t) != _DESC.size:
+        raise ImportError("mla_tensor_t layout does not match the packed descriptor")
     P, T = ctypes.c_void_p, ctypes.POINTER(mla_tensor_t)
     lib.mla_decode_paged.argtypes = [T, T, P, T, T, ctypes.c_int32, ctypes.c_float, T, T, P]
     lib.mla_decode_paged.restype = ctypes.c_int
@@ -86,20 +89,20 @@ def lib() -> ctypes.CDLL:
     return _lib
 
 
+_DESC = struct.Struct("<Q5q5qii")  # the byte layout of mla_tensor_t
+_PAD = tuple((0,) * k for k in range(6))
+
+
 def describe(t: torch.Tensor | None):
     """torch tensor -> mla_tensor_t (no copy; the tensor must outlive the call)."""
     if t is None:
         return None
-    if t.dim() > 5:
+    n = t.dim()
+    if n > 5:
         raise ValueError("at most 5 dims")
-    d = mla_tensor_t()
-    d.data = t.data_ptr()
-    for i in range(t.dim()):
-        d.shape[i] = t.shape[i]
-        d.stride[i] = t.stride(i)
-    d.ndim = t.dim()
-    d.dtype = _DTYPES.get(t.dtype, 0)
-    return d
+    pad = _PAD[5 - n]
+    return mla_tensor_t.from_buffer_copy(_DESC.pack(t.data_ptr(), *t.shape, *pad, *t.stride(), *pad, n,
+                                                    _DTYPES.get(t.dtype, 0)))
 
 
 def _ref(d):

@@ -1059,8 +1059,18 @@ cudaError_t launch_tc_decode(const DecodeParams& p, cudaStream_t stream, bool* h
     }
     if (!tc_supports(p, cc[dev][0], cc[dev][1])) return cudaSuccess;
 
-    CUtensorMap map, map_box;
-    if ((e = encode_cache_maps(&map, &map_box, p.kv, p.num_pages)) != cudaSuccess) return e;
+    // The two maps depend only on the cache's address and page count; a
+    // serving loop passes the same cache every step, so keep the last pair
+    // this thread encoded (addresses are unique across devices).
+    thread_local const uint8_t* map_kv = nullptr;
+    thread_local int64_t map_pages = -1;
+    thread_local CUtensorMap map, map_box;
+    if (p.kv != map_kv || p.num_pages != map_pages) {
+        map_kv = nullptr;
+        if ((e = encode_cache_maps(&map, &map_box, p.kv, p.num_pages)) != cudaSuccess) return e;
+        map_kv = p.kv;
+        map_pages = p.num_pages;
+    }
     const int HT = p.H * p.T;
     // G CTAs (16 rows each) per (partition, request), adjacent in the grid
     const unsigned G = HT <= kNq ? 1u : static_cast<unsigned>((HT + kNq - 1) / kNq);
