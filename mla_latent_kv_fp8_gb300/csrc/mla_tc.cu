@@ -21,19 +21,23 @@
 //     K_page[64 x 576] . [q1 | q2]^T (M=64, N=32).  PV: for each 128-dim block of
 //     the latent, D[128 dims x 32] = V^T[128 x 64 pos] . [p1 | p2]^T, with V^T read
 //     from the same page tile as an MN-major operand (M=128, N=32).
-//   * Probabilities are scaled per tile: P = 2^(s - m_tile) in [0, 1], stored as
-//     two e4m3 terms p1 + p2 / 16 of 256 * P (relative error ~2^-8, the bf16
-//     level); the running output, max and normaliser live in registers of the
-//     correction warps and absorb each tile with exact fp32 LSE rescaling.
-//   * Warp roles: warp 0 TMA producer; three MMA-issuing threads (warp 1: QK^T of
+//   * Probabilities are taken against a per-head reference r that moves only
+//     when a score would exceed r + 8 (log2 units): P = 2^(s - r) in (0, 256],
+//     stored as two e4m3 terms p1 + p2 / 16 (relative error ~2^-8, the bf16
+//     level).  Each lane first compares its own scores with r; one named
+//     barrier ORs that test over the warpgroup, and only when it is set do the
+//     warps reduce the page maxima and move r (new r = page max - 4), rescaling
+//     the accumulated output in TMEM in place.  Most pages skip the reductions.
+//   * Warp roles: warp 0 TMA producer; three MMA-issuing warps (warp 1: QK^T of
 //     even pages, warp 3: QK^T of odd pages, warp 2: PV of every page), because
 //     one thread can issue a tcgen05.mma only every ~50 cycles; and two
-//     attention warpgroups (warps 4-7, 8-11) that take alternate pages.  For its page a warpgroup reads the score tile (TMEM lane =
-//     position), computes the tile softmax, hands the quantised probabilities
-//     to the PV issuer and, after PV, folds the output tile (TMEM lane = latent
-//     dim) into its own running output; each thread also keeps fp32 partial
-//     normalisers of its positions, rescaled with the same factors.  The two
-//     running states are merged once at the end.
+//     attention warpgroups (warps 4-7, 8-11) that take alternate pages.  For
+//     its page a warpgroup reads the score tile (TMEM lane = position), forms
+//     the probabilities and hands them to the PV issuer; PV accumulates into
+//     that warpgroup's own output tile in TMEM (lane = latent dim) over all of
+//     its pages.  Each thread keeps fp32 partial normalisers of its positions.
+//   * At the end the warpgroup without the last page parks its tile in a free
+//     page slot; the other combines it with its own and stores the rows.
 //   * Every wait is bounded; on timeout the kernel records an error, drains its
 //     own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -78,8 +82,7 @@ struct Smem {
     uint8_t pp[kGroups][2][kPpBytes];        // [p1 | p2] MN-major, no swizzle, per group page
     float red_m[kGroups][2][kNq][4];         // [group][iter parity][head][warp] tile maxima
     float red_l[kGroups][kNq][4];            // per group: end-of-loop normaliser partials
-    float fin[kGroups][2][kNq];              // per group: final max / normaliser by head
-    float wrow[kGroups][kNq];                // final weight of each group's tile, by head
+    float fin[2][kNq];                       // parked warpgroup: final reference / normaliser by head
     alignas(16) float row_scale[kNq];        // kv_scale * sm_scale * log2(e) * 2^-e
     alignas(16) int rowlim[kNq];             // visible prefix per row; -1 = padding
     uint64_t full[kStages], empty[kStages];
@@ -694,7 +697,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool page_ok = pid >= 0 && pid < p.num_pages;
             const int pos = (pg_begin + i) * kPage + pr;
             float s[kHL];
-            // ---- scores of this page; this warp's maximum of each head ----
+            bool over = false;  // a score of this lane exceeds its head's reference + headroom
+            // ---- scores of this page ----
             if (!fail) fail = !warp_wait(&S.s_full[sb], (i / kSBufs) & 1, abort, p.err);
             if (!fail) {
                 tc_fence_after();
@@ -707,7 +711,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&S.s_empty[sb]);
                 const bool in_part = page_ok && pos < p_end;
-                float mine = NEG;  // lanes 8*half + j (j < 8): this warp's max of head 8*half + j
 #pragma unroll
                 for (int j = 0; j < kHL; ++j) {
                     const int h = kHL * half + j;
@@ -717,55 +720,67 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float moved = __shfl_xor_sync(0xffffffffu, hi, 16);
                     const float v = (half ? moved : lo) * rsc[j];
                     s[j] = (h < kRows && in_part && (!causal || pos < S.rowlim[h])) ? v : NEG;
-                    // head j of half 0 and head 8 + j of half 1: one full-warp
-                    // reduction each, the other half contributing -inf
-                    const float wlo = warp_max_redux(half ? NEG : s[j]);
-                    const float whi = warp_max_redux(half ? s[j] : NEG);
-                    mine = ((lane & 15) == j) ? (half ? whi : wlo) : mine;
+                    over |= s[j] > rr[j] + kHeadroom;  // rr = -inf: any score moves it
                 }
-                if ((lane & 15) < kHL) S.red_m[g][kb][kHL * half + (lane & 15)][quad] = mine;  // rows >= kRows: -inf
             }
-            if (group_sync_or(g, fail)) {
-                fail = true;
-                break;
-            }
-            // ---- page maxima; move the reference where a score would overflow ----
-            float t = NEG;
-            if (lane < kNq) {
-                const float4 vm = *reinterpret_cast<const float4*>(S.red_m[g][kb][lane]);
-                t = fmaxf(fmaxf(vm.x, vm.y), fmaxf(vm.z, vm.w));
-            }
-            const bool need = lane < kRows && t > r_l + kHeadroom;
-            if (__ballot_sync(0xffffffffu, need)) {
-                const float rn = need ? t - kShift : r_l;
-                const float a = need ? exp2f(r_l - rn) : 1.f;  // r_l = -inf: nothing to keep
-                r_l = rn;
+            // One barrier per page decides whether any head's reference moves;
+            // only then do the warps exchange their page maxima (a second
+            // barrier), so most pages skip the max reductions entirely.
+            if (group_sync_or(g, fail || over)) {
+                if (!fail) {
+                    float mine = NEG;  // lanes 8*half + j (j < 8): this warp's max of head 8*half + j
 #pragma unroll
-                for (int j = 0; j < kHL; ++j) {
-                    rr[j] = __shfl_sync(0xffffffffu, rn, kHL * half + j);
-                    lp[j] *= __shfl_sync(0xffffffffu, a, kHL * half + j);
+                    for (int j = 0; j < kHL; ++j) {
+                        // head j of half 0 and head 8 + j of half 1: one full-warp
+                        // reduction each, the other half contributing -inf
+                        const float wlo = warp_max_redux(half ? NEG : s[j]);
+                        const float whi = warp_max_redux(half ? s[j] : NEG);
+                        mine = ((lane & 15) == j) ? (half ? whi : wlo) : mine;
+                    }
+                    if ((lane & 15) < kHL) S.red_m[g][kb][kHL * half + (lane & 15)][quad] = mine;  // rows >= kRows: -inf
                 }
+                if (group_sync_or(g, fail)) {
+                    fail = true;
+                    break;
+                }
+                // ---- page maxima; move the reference where a score would overflow ----
+                float t = NEG;
+                if (lane < kNq) {
+                    const float4 vm = *reinterpret_cast<const float4*>(S.red_m[g][kb][lane]);
+                    t = fmaxf(fmaxf(vm.x, vm.y), fmaxf(vm.z, vm.w));
+                }
+                const bool need = lane < kRows && t > r_l + kHeadroom;
+                if (__ballot_sync(0xffffffffu, need)) {
+                    const float rn = need ? t - kShift : r_l;
+                    const float a = need ? exp2f(r_l - rn) : 1.f;  // r_l = -inf: nothing to keep
+                    r_l = rn;
+#pragma unroll
+                    for (int j = 0; j < kHL; ++j) {
+                        rr[j] = __shfl_sync(0xffffffffu, rn, kHL * half + j);
+                        lp[j] *= __shfl_sync(0xffffffffu, a, kHL * half + j);
+                    }
 
-                if (k > 0) {
-                    // The tile holds PV of this group's pages 0..k-1: wait for the
-                    // last of them, then scale every head's columns.
-                    if (!warp_wait(&S.pv_done[g][(k - 1) & 1], ((k - 1) >> 1) & 1, abort, p.err)) {
-                        fail = true;
-                    } else {
-                        tc_fence_after();
+                    if (k > 0) {
+                        // The tile holds PV of this group's pages 0..k-1: wait for the
+                        // last of them, then scale every head's columns.
+                        if (!warp_wait(&S.pv_done[g][(k - 1) & 1], ((k - 1) >> 1) & 1, abort, p.err)) {
+                            fail = true;
+                        } else {
+                            tc_fence_after();
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            uint32_t v[32];
-                            tmem_ld32(to + 32 * c, v);
-                            tmem_wait_ld();
+                            for (int c = 0; c < 4; ++c) {
+                                uint32_t v[32];
+                                tmem_ld32(to + 32 * c, v);
+                                tmem_wait_ld();
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) {
-                                const float al = __shfl_sync(0xffffffffu, a, j & 15);  // lane h: head h
-                                if ((j & 15) < kRows) v[j] = __float_as_uint(__uint_as_float(v[j]) * al);
+                                for (int j = 0; j < 32; ++j) {
+                                    const float al = __shfl_sync(0xffffffffu, a, j & 15);  // lane h: head h
+                                    if ((j & 15) < kRows) v[j] = __float_as_uint(__uint_as_float(v[j]) * al);
+                                }
+                                tmem_st32(to + 32 * c, v);
                             }
-                            tmem_st32(to + 32 * c, v);
+                            tmem_wait_st();
                         }
-                        tmem_wait_st();
                     }
                 }
             }
@@ -846,114 +861,75 @@ __global__ void __launch_bounds__(kThreads, 1)
             l_run = (vl.x + vl.y) + (vl.z + vl.w);
         }
 
-        // ---- merge the warpgroups' running states; write the answer ----
-        // Both warpgroups park their tiles as [row][512] fp32 in page slots that
-        // no copy or MMA touches any more (warpgroup 1: the slot of its own last
-        // page, or an unused one; warpgroup 0: the next slot).  Each then merges
-        // half of the rows in place into warpgroup 0's tile, and the answer rows
-        // leave in one bulk copy (they are contiguous in global memory).  The
-        // eight warps meet at named barrier 4, each exactly three times.
-        static_assert(kGroups == 2, "the staging slots assume two warpgroups");
-        const int sl_park = [&] {
-            const int c1 = n_pages > 1 ? (n_pages - 1 + kGroups - 1) / kGroups : 0;
-            return c1 > 0 ? (1 + kGroups * (c1 - 1)) % kStages : kStages - 1;
-        }();
-        float* tile1 = reinterpret_cast<float*>(S.slot[sl_park]);
-        float* tile0 = reinterpret_cast<float*>(S.slot[(sl_park + 1) % kStages]);
-        __nv_bfloat16* stage_bf = reinterpret_cast<__nv_bfloat16*>(S.slot[(sl_park + 2) % kStages]);
-        {
-            float* mine = g == 0 ? tile0 : tile1;
+        // ---- combine the warpgroups' running states; write the answer ----
+        // The warpgroup that owns the partition's last page finishes last.  The
+        // other one parks its tile as [row][512] fp32, with its references and
+        // normalisers, in the slot of its own last page (or in a slot no page
+        // used) and leaves; the last one combines that tile with its own
+        // registers and stores the answer rows straight to global memory.
+        static_assert(kGroups == 2, "the parking slot assumes two warpgroups");
+        const int gc = (n_pages - 1) % kGroups;  // combining warpgroup (n_pages >= 1 here)
+        const int gp = 1 - gc;                   // parking warpgroup
+        const int cnt_p = n_pages > gp ? (n_pages - gp + kGroups - 1) / kGroups : 0;
+        float* tile = reinterpret_cast<float*>(S.slot[cnt_p > 0 ? (gp + kGroups * (cnt_p - 1)) % kStages : kStages - 1]);
+        if (g == gp) {
 #pragma unroll
             for (int c = 0; c < 4; ++c)
 #pragma unroll
-                for (int h = 0; h < kRows; ++h) mine[h * kDv + 128 * c + d] = o[c][h];
+                for (int h = 0; h < kRows; ++h) tile[h * kDv + 128 * c + d] = o[c][h];
             if (quad == 0 && lane < kNq) {
-                S.fin[g][0][lane] = m_run;
-                S.fin[g][1][lane] = l_run;
+                S.fin[0][lane] = m_run;
+                S.fin[1][lane] = l_run;
             }
-        }
-        asm volatile("bar.sync 4, 256;" ::: "memory");  // both tiles and states parked
-        const bool direct = p.n_splits == 1;
-        if (g == 0 && quad == 0 && lane < kNq) {
+            __threadfence_block();
+            asm volatile("bar.arrive 4, 256;" ::: "memory");  // tile and state parked
+        } else {
+            asm volatile("bar.sync 4, 256;" ::: "memory");
+            const bool direct = p.n_splits == 1;
             // lane h: the weight of each tile (normaliser and kv_scale folded in)
-            const float m0 = S.fin[0][0][lane], l0 = S.fin[0][1][lane];
-            const float m1 = S.fin[1][0][lane], l1 = S.fin[1][1][lane];
-            const float mn = fmaxf(m0, m1);
-            float w0 = 0.f, w1 = 0.f, l = 0.f;
-            if (mn != NEG) {
-                w0 = exp2f(m0 - mn);
-                w1 = exp2f(m1 - mn);
-                l = l0 * w0 + l1 * w1;
-            }
-            const float inv = (l > 0.f) ? kv_scale / l : 0.f;
-            S.wrow[0][lane] = w0 * inv;
-            S.wrow[1][lane] = w1 * inv;
-            if (lane < HTc) {
-                const float lse = (l > 0.f) ? (mn + log2f(l)) * kLn2 : -INFINITY;
-                const int64_t grow = (int64_t)b * HT + r0 + lane;
-                if (direct) {
-                    if (p.lse) p.lse[grow] = lse;
-                } else {
-                    p.part_lse[(int64_t)split * p.B * HT + grow] = lse;
+            float w_own = 0.f, w_park = 0.f;
+            if (lane < kNq) {
+                const float mp = S.fin[0][lane], lq = S.fin[1][lane];
+                const float mn = fmaxf(m_run, mp);
+                float l = 0.f;
+                if (mn != NEG) {
+                    w_own = exp2f(m_run - mn);
+                    w_park = exp2f(mp - mn);
+                    l = l_run * w_own + lq * w_park;
+                }
+                const float inv = (l > 0.f) ? kv_scale / l : 0.f;
+                w_own *= inv;
+                w_park *= inv;
+                if (quad == 0 && lane < HTc) {
+                    const float lse = (l > 0.f) ? (mn + log2f(l)) * kLn2 : -INFINITY;
+                    const int64_t grow = (int64_t)b * HT + r0 + lane;
+                    if (direct) {
+                        if (p.lse) p.lse[grow] = lse;
+                    } else {
+                        p.part_lse[(int64_t)split * p.B * HT + grow] = lse;
+                    }
                 }
             }
-        }
-        asm volatile("bar.sync 4, 256;" ::: "memory");  // weights
-        {
-            // Rows [g * kHalf, g * kHalf + kHalf) of this warpgroup: every load first.
-            constexpr int kHalf = (kRows + 1) / 2;
-            float w0[kHalf], w1[kHalf], t0[kHalf][4], t1[kHalf][4];
+            // every load of the parked tile first, then every store
 #pragma unroll
-            for (int j = 0; j < kHalf; ++j) {
-                const int h = g * kHalf + j;
-                w0[j] = S.wrow[0][h < kNq ? h : 0];
-                w1[j] = S.wrow[1][h < kNq ? h : 0];
+            for (int h = 0; h < kRows; ++h) {
+                const float wo = __shfl_sync(0xffffffffu, w_own, h);
+                const float wp = __shfl_sync(0xffffffffu, w_park, h);
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    t0[j][c] = h < HTc ? tile0[h * kDv + 128 * c + d] : 0.f;
-                    t1[j][c] = h < HTc ? tile1[h * kDv + 128 * c + d] : 0.f;
-                }
+                for (int c = 0; c < 4; ++c) o[c][h] = fmaf(tile[h * kDv + 128 * c + d], wp, o[c][h] * wo);
             }
-#pragma unroll
-            for (int j = 0; j < kHalf; ++j) {
-                const int h = g * kHalf + j;
-                if (h >= HTc) break;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const float v = fmaf(t1[j][c], w1[j], t0[j][c] * w0[j]);
-                    if (direct)
-                        stage_bf[h * kDv + 128 * c + d] = __float2bfloat16_rn(v);
-                    else
-                        tile0[h * kDv + 128 * c + d] = v;
-                }
-            }
-        }
-        fence_async_smem();  // staged rows: generic writes -> bulk-copy reads
-        asm volatile("bar.sync 4, 256;" ::: "memory");  // answer rows staged
-        if (g == 0) {
-            const int n = HTc * kDv;
             const int64_t row0 = (int64_t)b * HT + r0;  // this CTA's first answer row
-            void* dst = direct ? static_cast<void*>(p.out + row0 * kDv)
-                               : static_cast<void*>(p.part_out + ((int64_t)split * p.B * HT + row0) * kDv);
-            const void* src = direct ? static_cast<const void*>(stage_bf) : static_cast<const void*>(tile0);
-            const uint32_t bytes = static_cast<uint32_t>(n) * (direct ? 2u : 4u);
-            if ((reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
-                if (tid == 128 && bytes > 0) {
-                    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
-                                     reinterpret_cast<uint64_t>(dst)),
-                                 "r"(smem_u32(src)), "r"(bytes)
-                                 : "memory");
-                    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-                    // Only the shared-memory reads must finish before the CTA
-                    // leaves; the writes complete with the grid.
-                    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-                }
-            } else {  // destination not 16-byte aligned: plain stores
-                for (int idx = tid - 128; idx < n; idx += 128) {
-                    if (direct)
-                        static_cast<__nv_bfloat16*>(dst)[idx] = stage_bf[idx];
-                    else
-                        static_cast<float*>(dst)[idx] = tile0[idx];
+#pragma unroll
+            for (int h = 0; h < kRows; ++h) {
+                if (h < HTc) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int64_t at = (row0 + h) * kDv + 128 * c + d;
+                        if (direct)
+                            p.out[at] = __bfloat16_as_ushort(__float2bfloat16_rn(o[c][h]));
+                        else
+                            p.part_out[(int64_t)split * p.B * HT * kDv + at] = o[c][h];
+                    }
                 }
             }
         }
