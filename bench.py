@@ -44,6 +44,7 @@ def parse():
     ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tcgen05"])
     ap.add_argument("--n-splits", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-ceiling", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -91,6 +92,36 @@ def carve(device, specs, pin=False):
         es = torch.empty((), dtype=dtype).element_size()
         views.append(buf[o:o + n * es].view(dtype).view(shape))
     return buf, views
+
+
+def stream_ceiling(L, base, caches, n_copies, grid, stream, launches=200):
+    """Time the library's page-streaming probe on the pages one decode step reads:
+    every page of every request once, split evenly over the decode's grid, through
+    the same TMA ring, with no arithmetic.  Its GB/s is the ceiling of this access
+    pattern at this launch size (ramp-up and tail included)."""
+    import torch
+    n_req = ((base.seq_lens.long() + 63) // 64).cpu()
+    ids = torch.cat([base.block_table[b, :int(n_req[b])] for b in range(base.block_table.shape[0])])
+    ctas = max(1, min(grid, ids.numel()))
+    ppc = ids.numel() // ctas
+    ids = ids[:ctas * ppc].contiguous()
+    for i in range(3):
+        L.mla_bench_stream_pages(caches[i % n_copies], ids, ctas, ppc, stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(launches):
+        L.mla_bench_stream_pages(caches[i % n_copies], ids, ctas, ppc, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if L.mla_device_error() != 0:
+        raise RuntimeError("page-streaming probe reported a device error")
+    us = e0.elapsed_time(e1) * 1e3 / launches
+    nbytes = ids.numel() * 64 * 576
+    return {"value": round(nbytes / (us * 1e-6) / 1e9, 1), "unit": "GB/s", "us_per_launch": round(us, 2),
+            "ctas": ctas, "pages_per_cta": ppc, "bytes_per_launch": nbytes, "launches": launches,
+            "note": "mla_bench_stream_pages: the step's pages copied through the decode's TMA ring "
+                    "and discarded, back-to-back launches"}
 
 
 def source_sha(rel_path):
@@ -285,6 +316,11 @@ def run_ours(args):
                 "frac_of_8TBps": round(achieved / HBM_NOMINAL_GBS, 4),
                 "algorithmic_bytes_per_launch": kv_bytes}
 
+    # ---- the ceiling of this access pattern: the same pages, no arithmetic ----
+    ceiling = None
+    if not args.no_ceiling:
+        ceiling = stream_ceiling(L, base, caches, n_copies, B * n_eff * -(-(H * T) // 16), stream)
+
     # ---- end to end through the C ABI with host buffers ----
     e2e = None
     if not args.no_e2e:
@@ -357,6 +393,7 @@ def run_ours(args):
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
+            "stream_ceiling": ceiling,
             "gpu_launches": args.steps * (1 + (1 if n_eff > 1 else 0)),
             "clocks": clocks,
         }

@@ -124,8 +124,9 @@ mla_status_t mla_decode_paged(const mla_tensor_t *q, const mla_tensor_t *kv_cach
  * their normalisers (section 1, DCP merge):
  *     lse = M + ln sum_s exp(lse_s - M),  M = max_s lse_s,
  *     out = sum_s exp(lse_s - lse) * partial_out_s.
- * Shards with lse_s = -inf weigh 0 and their partial_out is not read; rows
- * whose every shard is -inf get out = 0, lse = -inf.
+ * Shards with lse_s = -inf weigh 0 and their partial_out values are ignored
+ * (whatever bits they hold, NaN included); rows whose every shard is -inf get
+ * out = 0, lse = -inf.
  *
  *   partial_out bf16 or fp32 [S, B, T, H, 512] (any rank >= 2 whose first dim
  *               is S and last dim 512), device, contiguous.

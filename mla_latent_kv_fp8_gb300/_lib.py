@@ -28,7 +28,7 @@ _DTYPES = {torch.bfloat16: 1, torch.float32: 2, torch.uint8: 3, torch.float8_e4m
 EXPORTS = ("mla_decode_paged", "mla_merge_partials", "mla_auto_splits", "mla_split_chunk_pages",
            "mla_decode_workspace_bytes", "mla_set_impl", "mla_device_error", "mla_status_string",
            "mla_last_error", "mla_profile_next_decode", "mla_last_decode_impl",
-           "mla_decode_paged_noalloc", "mla_test_stall_copies")
+           "mla_decode_paged_noalloc", "mla_test_stall_copies", "mla_bench_stream_pages")
 
 
 class MlaError(RuntimeError):
@@ -66,6 +66,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mla_set_impl.restype = ctypes.c_int32
     lib.mla_test_stall_copies.argtypes = [ctypes.c_int]
     lib.mla_test_stall_copies.restype = ctypes.c_int
+    lib.mla_bench_stream_pages.argtypes = [P, ctypes.c_int64, P, ctypes.c_int32, ctypes.c_int32, P]
+    lib.mla_bench_stream_pages.restype = ctypes.c_int
     lib.mla_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32), P]
     lib.mla_device_error.restype = ctypes.c_int
     lib.mla_last_decode_impl.argtypes = []
@@ -170,6 +172,14 @@ def mla_test_stall_copies(on: bool) -> int:
     copies, so their bounded waits run out (device error 1).  Returns the
     previous setting."""
     return lib().mla_test_stall_copies(1 if on else 0)
+
+
+def mla_bench_stream_pages(kv_cache, page_ids, ctas, pages_per_cta, stream=None):
+    """Benchmark instrumentation: stream the given pages of the cache through the
+    decode kernel's TMA ring with no arithmetic (the HBM ceiling of that pattern)."""
+    _check(lib().mla_bench_stream_pages(ctypes.c_void_p(kv_cache.data_ptr()), int(kv_cache.shape[0]),
+                                        ctypes.c_void_p(page_ids.data_ptr()), int(ctas), int(pages_per_cta),
+                                        _stream(stream)))
 
 
 def mla_last_decode_impl() -> int:

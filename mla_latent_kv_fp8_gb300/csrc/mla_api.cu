@@ -12,6 +12,7 @@
 #include <utility>
 
 #include "../../include/mla_decode.h"
+#include "../../include/mla_decode_testing.h"
 #include "mla_internal.cuh"
 
 // The device error word written by kernels (bounded waits, bounds checks).
@@ -424,3 +425,22 @@ mla_status_t mla_merge_partials(const mla_tensor_t* partial_out, const mla_tenso
 }
 
 }  // extern "C"
+
+int mla_bench_stream_pages(const void* kv_cache, int64_t num_pages, const int32_t* page_ids, int32_t ctas,
+                           int32_t pages_per_cta, void* stream) {
+    using namespace mla;
+    if (!kv_cache || !page_ids) return fail(MLA_ERR_INVALID_ARG, "mla_bench_stream_pages: null pointer");
+    if ((reinterpret_cast<uintptr_t>(kv_cache) & 15) != 0)
+        return fail(MLA_ERR_INVALID_ARG, "mla_bench_stream_pages: kv_cache must be 16-byte aligned");
+    if (num_pages < 1 || num_pages * kPage >= (int64_t(1) << 31))
+        return fail(MLA_ERR_INVALID_ARG, "mla_bench_stream_pages: num_pages out of range");
+    if (ctas < 1 || ctas > 65535 || pages_per_cta < 1)
+        return fail(MLA_ERR_INVALID_ARG, "mla_bench_stream_pages: ctas in [1, 65535], pages_per_cta >= 1");
+    DeviceInfo* dev = nullptr;
+    mla_status_t st = device_info(&dev);
+    if (st != MLA_OK) return st;
+    cudaError_t e = launch_stream_probe(static_cast<const uint8_t*>(kv_cache), num_pages, page_ids, ctas,
+                                        pages_per_cta, dev->err_word, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "stream probe launch");
+    return MLA_OK;
+}

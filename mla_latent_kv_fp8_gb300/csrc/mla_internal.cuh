@@ -59,5 +59,7 @@ struct MergeParams {
 
 cudaError_t launch_simt_decode(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
+cudaError_t launch_stream_probe(const uint8_t* kv, int64_t num_pages, const int32_t* page_ids, int ctas,
+                                int pages_per_cta, int* err, cudaStream_t stream);
 
 }  // namespace mla

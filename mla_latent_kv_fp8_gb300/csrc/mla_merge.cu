@@ -7,7 +7,7 @@
 // normaliser of part s:
 //     lse = M + ln sum_s exp(lse_s - M),   M = max_s lse_s
 //     out = sum_s exp(lse_s - lse) * o_s
-// Parts with lse_s = -inf weigh exactly 0 and are not read.
+// Parts with lse_s = -inf weigh exactly 0; their values are never multiplied.
 //
 // Two kernels:
 //   * few parts (S <= 32): one warp per (row, 64 value dims); lane s holds

@@ -84,93 +84,73 @@ __device__ __forceinline__ void merge_warp(const MergeParams& p, int64_t row, in
     if (chunk == 0 && lane == 0 && p.lse) p.lse[row] = M + logf(sum);
 }
 
-// Normalisers of up to kSmemParts parts are kept in shared memory; beyond that
-// they are re-read from global memory (a slow path for very many parts).
-constexpr int kSmemParts = 1024;
-constexpr int kFirstRound = 32;  // parts per warp whose values load with the normalisers
-
 struct CtaScratch {             // shared memory of merge_cta
-    float lse[kSmemParts];
-    float red[8];
-    float part[8][32];
+    float m[8];                 // per warp: maximum normaliser of its parts
+    float l[8];                 // per warp: sum of exp(lse_s - m) over its parts
+    float part[8][32];          // per warp and dim: sum of exp(lse_s - m) * o_s
 };
 
-// Many parts (S > 32): 256 threads (eight warps, synchronised by `sync`) merge
-// (row, 32 value dims chunk); the warps split the parts, each lane owns one
-// dim; the values of the first 256 parts load in the same round as the
-// normalisers, and the warps' sums meet in shared memory.  Every thread of the
-// eight warps takes the same path.
+// Many parts (S > 32): 256 threads (eight warps) merge (row, 32 value dims).
+// Warp w takes parts w, w + 8, w + 16, ...; each lane owns one dim.  A warp
+// loads 32 of its parts' normalisers (one per lane) together with their values,
+// so a round costs one memory latency, and merges them against its own
+// maximum; parts beyond 256 take further rounds, folded in by rescaling.  The
+// eight warps' results meet once in shared memory (one `sync`).
 template <bool kBf16In, class Sync>
 __device__ __forceinline__ void merge_cta(const MergeParams& p, int64_t row, int chunk, int tid, CtaScratch& sh,
                                           Sync sync) {
     const int lane = tid & 31, wid = tid >> 5;
     const int col = chunk * 32 + lane;
-    auto lse_at = [&](int s) { return s < kSmemParts ? sh.lse[s] : p.part_lse[(int64_t)s * p.rows + row]; };
-
-    float v[kFirstRound];
+    float m_w = -INFINITY, l_w = 0.f, acc = 0.f;
+    for (int base = 0; base < p.S; base += 256) {
+        float v[32];
 #pragma unroll
-    for (int k = 0; k < kFirstRound; ++k) {
-        const int s = wid + 8 * k;
-        v[k] = s < p.S ? load1<kBf16In>(p.part_out, ((int64_t)s * p.rows + row) * kDv + col) : 0.f;
-    }
-    sync();  // the previous use of the scratch is over
-    float mx = -INFINITY;
-    for (int s = tid; s < p.S; s += 256) {
-        const float l = p.part_lse[(int64_t)s * p.rows + row];
-        if (s < kSmemParts) sh.lse[s] = l;
-        mx = fmaxf(mx, l);
-    }
-    mx = warp_max(mx);
-    if (lane == 0) sh.red[wid] = mx;
-    sync();
-    float M = sh.red[0];
-#pragma unroll
-    for (int i = 1; i < 8; ++i) M = fmaxf(M, sh.red[i]);
-    sync();
-    if (M == -INFINITY) {
-        if (wid == 0) {
-            p.out[row * kDv + col] = 0;
-            if (chunk == 0 && lane == 0 && p.lse) p.lse[row] = -INFINITY;
+        for (int k = 0; k < 32; ++k) {
+            const int s = base + wid + 8 * k;
+            v[k] = s < p.S ? load1<kBf16In>(p.part_out, ((int64_t)s * p.rows + row) * kDv + col) : 0.f;
         }
-        return;
-    }
-    float sm = 0.f;
-    for (int s = tid; s < p.S; s += 256) {
-        const float ls = lse_at(s);
-        if (ls != -INFINITY) sm += exp2f((ls - M) * kLog2e);
-    }
-    sm = warp_sum(sm);
-    if (lane == 0) sh.red[wid] = sm;
-    sync();
-    float sum = 0.f;
+        const int sl = base + wid + 8 * lane;  // this lane's part for the normalisers
+        const float ls = sl < p.S ? p.part_lse[(int64_t)sl * p.rows + row] : -INFINITY;
+        const float mr = warp_max(ls);
+        if (mr == -INFINITY) continue;  // warp-uniform: no part of this round counts
+        const float mn = fmaxf(m_w, mr);
+        const float a = (m_w == -INFINITY) ? 0.f : exp2f((m_w - mn) * kLog2e);
+        const float e = (ls == -INFINITY) ? 0.f : exp2f((ls - mn) * kLog2e);
+        float r = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) sum += sh.red[i];
-    const float lse_out = M + logf(sum);
-
-    float acc = 0.f;
-#pragma unroll
-    for (int k = 0; k < kFirstRound; ++k) {
-        const int s = wid + 8 * k;
-        if (s < p.S) {
-            const float ls = lse_at(s);
-            if (ls != -INFINITY) acc = fmaf(exp2f((ls - lse_out) * kLog2e), v[k], acc);
+        for (int k = 0; k < 32; ++k) {
+            const float ek = __shfl_sync(0xffffffffu, e, k);
+            if (ek != 0.f) r = fmaf(ek, v[k], r);  // a part of weight 0 is never multiplied
         }
+        acc = fmaf(acc, a, r);
+        l_w = fmaf(l_w, a, warp_sum(e));
+        m_w = mn;
     }
-    for (int s = wid + 8 * kFirstRound; s < p.S; s += 8) {  // beyond 256 parts
-        const float ls = lse_at(s);
-        if (ls != -INFINITY)
-            acc = fmaf(exp2f((ls - lse_out) * kLog2e), load1<kBf16In>(p.part_out, ((int64_t)s * p.rows + row) * kDv + col),
-                       acc);
+    if (lane == 0) {
+        sh.m[wid] = m_w;
+        sh.l[wid] = l_w;
     }
     sh.part[wid][lane] = acc;
     sync();
     if (wid == 0) {
-        float t = 0.f;
+        float M = sh.m[0];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) t += sh.part[i][lane];
-        __nv_bfloat16 o = __float2bfloat16_rn(t);
+        for (int i = 1; i < 8; ++i) M = fmaxf(M, sh.m[i]);
+        if (M == -INFINITY) {
+            p.out[row * kDv + col] = 0;
+            if (chunk == 0 && lane == 0 && p.lse) p.lse[row] = -INFINITY;
+            return;
+        }
+        float sum = 0.f, t = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float f = (sh.m[i] == -INFINITY) ? 0.f : exp2f((sh.m[i] - M) * kLog2e);
+            sum = fmaf(sh.l[i], f, sum);
+            t = fmaf(sh.part[i][lane], f, t);
+        }
+        __nv_bfloat16 o = __float2bfloat16_rn(t / sum);
         p.out[row * kDv + col] = *reinterpret_cast<uint16_t*>(&o);
-        if (chunk == 0 && lane == 0 && p.lse) p.lse[row] = lse_out;
+        if (chunk == 0 && lane == 0 && p.lse) p.lse[row] = M + logf(sum);
     }
 }
 

@@ -166,3 +166,15 @@ def test_binding_maps_torch_dtypes(L):
     assert L.describe(torch.zeros(1, dtype=torch.float8_e4m3fn)).dtype == 3
     assert L.describe(torch.zeros(1, dtype=torch.int32)).dtype == 4
     assert L.describe(None) is None
+
+
+def test_stream_probe_rejects_bad_arguments_on_host(L):
+    lib = L.lib()
+    ids = ctypes.c_void_p(4096)  # never dereferenced: every case fails validation first
+    assert lib.mla_bench_stream_pages(None, 8, ids, 1, 1, None) == 1
+    assert lib.mla_bench_stream_pages(ctypes.c_void_p(4096), 8, None, 1, 1, None) == 1
+    assert lib.mla_bench_stream_pages(ctypes.c_void_p(4100), 8, ids, 1, 1, None) == 1   # not 16-byte aligned
+    assert lib.mla_bench_stream_pages(ctypes.c_void_p(4096), 0, ids, 1, 1, None) == 1   # no pages
+    assert lib.mla_bench_stream_pages(ctypes.c_void_p(4096), 1 << 25, ids, 1, 1, None) == 1
+    assert lib.mla_bench_stream_pages(ctypes.c_void_p(4096), 8, ids, 0, 1, None) == 1   # no CTAs
+    assert lib.mla_bench_stream_pages(ctypes.c_void_p(4096), 8, ids, 1, 0, None) == 1

@@ -180,7 +180,7 @@ def test_dcp_shards_merge_to_unsharded(L, impl):
 # mla_merge_partials on its own
 # ----------------------------------------------------------------------------
 
-@pytest.mark.parametrize("S", [1, 2, 8, 32, 33, 100])
+@pytest.mark.parametrize("S", [1, 2, 8, 32, 33, 100, 300, 1000])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 def test_merge_partials_matches_oracle(L, S, dtype):
     g = torch.Generator().manual_seed(S)
@@ -192,11 +192,15 @@ def test_merge_partials_matches_oracle(L, S, dtype):
     drop = torch.rand((S, *rows), generator=g) < 0.3
     pl[drop] = float("-inf")
     pl[:, 0, 0] = float("-inf")  # a row with every shard empty
+    empty = torch.isinf(pl)
+    po_ref = po.clone()
+    po_ref[empty] = 0
+    po[empty] = float("nan")  # the values of an empty shard are ignored, whatever they hold
     out = torch.full((*rows, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
     lse = torch.full(rows, float("nan"), dtype=torch.float32, device="cuda")
     L.mla_merge_partials(po.cuda(), pl.cuda(), S, out, lse)
     torch.cuda.synchronize()
-    ro, rl = oracle.merge(po.float().numpy().astype(np.float64), pl.numpy().astype(np.float64))
+    ro, rl = oracle.merge(po_ref.float().numpy().astype(np.float64), pl.numpy().astype(np.float64))
     assert_parity(out, lse, ro, rl, what=f"merge S={S}")
 
 
