@@ -168,8 +168,9 @@ mla_status_t mla_decode_paged_noalloc(const mla_tensor_t *q, const mla_tensor_t 
 /* The automatic split count used when n_splits == 0: enough history
  * partitions per request that B * splits fills every SM of the device
  * (at least one full wave), with at least 2 pages (128 positions) each.
- * When H * T > 16 every (request, partition) unit takes ceil(H * T / 16)
- * CTAs (16 rows each); the count then minimises the number of waves of CTAs
+ * Units of more than 16 rows run on the wide tensor-core kernel, 32 rows per
+ * CTA: a (request, partition) unit then takes ceil(H * T / 32) CTAs, and when
+ * that is more than one the count minimises the number of waves of CTAs
  * times the partition length.  Partitions never exceed 160 pages
  * (10,240 positions), so that in a batch of mixed lengths the longest request
  * does not bound the call.

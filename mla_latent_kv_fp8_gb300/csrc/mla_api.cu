@@ -188,9 +188,10 @@ constexpr int64_t kChunkCapPages = 160;  // 10,240 positions
 
 int32_t mla_auto_splits(int32_t B, int32_t T, int32_t H, int32_t max_pages, int32_t sm_count) {
     if (B <= 0 || max_pages <= 2) return 1;
-    // Rows (t, h) beyond 16 take ceil(rows / 16) CTAs per unit.
+    // Units of more than 16 rows (t, h) run on the wide kernel: ceil(rows / 32)
+    // CTAs per unit.
     const int64_t rows = (int64_t)(T > 0 ? T : 1) * (H > 0 ? H : 1);
-    const int64_t G = rows > 16 ? ceil_div(rows, 16) : 1;
+    const int64_t G = rows > 16 ? ceil_div(rows, 32) : 1;
     if (sm_count <= 0) {
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess ||

@@ -44,6 +44,10 @@ struct DecodeParams {
     float* part_lse;
     int* err;                   // device error word
     int test_stall_copies;      // failure-detection tests only: issue no page copies
+    // tcgen05 kernel for more than 16 rows: CTAs per (partition, request) and
+    // rows each (the last CTA may have fewer)
+    int row_ctas;
+    int rows_per_cta;
 };
 
 struct MergeParams {

@@ -50,6 +50,7 @@
 #include <mutex>
 
 #include "mla_internal.cuh"
+#include "mla_tc_ptx.cuh"
 
 namespace mla {
 namespace {
@@ -59,7 +60,8 @@ constexpr int kThreads = 128 + 128 * kGroups;
 constexpr int kStages = 5;                   // page slots in the TMA ring
 constexpr int kNq = 16;                      // rows (t, h) per CTA, padded
 constexpr int kNqk = 2 * kNq;                // MMA N: q1 rows | q2 rows (and p1 | p2)
-constexpr int kMaxRowsTc = 8 * kNq;          // rows beyond 16: up to 8 CTAs per partition
+constexpr int kMaxRowsTc = 128;             // rows beyond 16 go to the wide kernel
+constexpr int kWideRows = 32;               // rows per CTA of the wide kernel (at most 64)
 constexpr int kSlotBytes = kPage * kDqk;     // 36,864: one page
 constexpr int kBoxBytes = kPage * 64;        // 4,096: 64 positions x 64 dims
 constexpr int kBoxes = kDqk / 64;            // 9
@@ -70,7 +72,6 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSCol0 = 0;               // S buffers: 4 x 32 cols at [0, 128)
 constexpr uint32_t kSCols = 32;
 constexpr uint32_t kOCol0 = 128;             // O buffers: one per warpgroup, 128 cols each
-constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per wait
 constexpr float kHeadroom = 8.f;             // log2 units a score may exceed its head's reference
 constexpr float kShift = 4.f;                // a new reference sits this far below the page max
 static_assert(kOCol0 + 128 * kGroups <= kTmemCols, "TMEM budget");
@@ -96,214 +97,8 @@ struct Smem {
 };
 static_assert(sizeof(uint8_t[kStages][kSlotBytes]) % 1024 == 0, "slots keep 1 KB alignment");
 
-// ---------------------------------------------------------------- PTX wrappers
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-                 "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ float warp_max_redux(float v) {
-    float r;
-    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
-    return r;
-}
-__device__ __forceinline__ uint64_t global_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Wait for the phase of `parity` to complete, giving up after kTimeoutNs or
-// when another role has aborted.  Returns false on give-up.
-__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort, int* err) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 127u) == 0) {
-            if (*abort) return false;
-            if (global_ns() - t0 > kTimeoutNs) {
-                *abort = 1;
-                atomicCAS(err, 0, kErrWaitTimeout);
-                return false;
-            }
-        }
-    }
-}
-
-// Warp-wide bounded wait: every lane observes the phase flip itself (each lane
-// then holds its own acquire), and the warp agrees on the outcome.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* err) {
-    return __all_sync(0xffffffffu, wait_bounded(bar, parity, abort, err));
-}
-
-// One 64 x 64-byte box of a page (see encode_cache_maps).
-__device__ __forceinline__ void tma_load_box(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
-}
-// One whole page (see encode_cache_maps): a single copy instruction.
-__device__ __forceinline__ void tma_load_page(uint32_t dst, const CUtensorMap* map, int row, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row), "r"(0), "r"(smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void fence_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor (tcgen05): start, leading / stride byte
-// offsets, version 1, layout type (0 none, 4 = 64-byte swizzle).
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
-                                              uint32_t layout) {
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
-    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
-    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
-    d |= static_cast<uint64_t>(1) << 46;
-    d |= static_cast<uint64_t>(layout & 7u) << 61;
-    return d;
-}
-constexpr uint32_t kLayoutNone = 0;
-constexpr uint32_t kLayoutSw64 = 4;
-
-// Instruction descriptor, kind::f8f6f4, A = B = e4m3, D = f32.
-__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, bool a_mn_major, bool b_mn_major) {
-    return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
-           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
-}
 constexpr uint32_t kIdescQK = idesc_e4m3(64, kNqk, false, false);
 constexpr uint32_t kIdescPV = idesc_e4m3(128, kNqk, true, true);
-
-__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                         uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-            smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
-          "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
-          "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_wait_ld() {
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
-        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
-        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
-}
-__device__ __forceinline__ void tmem_wait_st() {
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-// True in exactly one lane of a converged warp.
-__device__ __forceinline__ bool elect_one() {
-    uint32_t pred;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t.reg .b32 r;\n\t"
-        "elect.sync r|p, 0xffffffff;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(pred));
-    return pred != 0;
-}
-
-// Barrier of the four warps of attention warpgroup g (named barrier 1 + g)
-// that also ORs a per-thread flag over them.  Shared-memory writes made before
-// it are visible to the group after it.
-__device__ __forceinline__ bool group_sync_or(int g, bool flag) {
-    uint32_t out;
-    __threadfence_block();
-    asm volatile(
-        "{\n\t.reg .pred pi, po;\n\t"
-        "setp.ne.u32 pi, %1, 0;\n\t"
-        "bar.red.or.pred po, %2, 128, pi;\n\t"
-        "selp.u32 %0, 1, 0, po;\n\t}"
-        : "=r"(out)
-        : "r"(flag ? 1u : 0u), "r"(1 + g)
-        : "memory");
-    return out != 0;
-}
-
-// e4m3 helpers (round to nearest even, saturating to +-448)
-__device__ __forceinline__ uint32_t f2_to_e4m3x2(float a, float b) {
-    return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
-}
-__device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t v) {
-    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v & 0xffffu), __NV_E4M3);
-    return __half22float2(*reinterpret_cast<__half2*>(&h));
-}
-
-// Byte offset of element (row n, k) in a K-major, no-swizzle operand made of
-// 8-row x 16-byte core matrices: LBO = 128 B along K, SBO = (K/16) * 128 along rows.
-__device__ __forceinline__ uint32_t kmajor_off(int n, int k, int K) {
-    return (n & 7) * 16 + (n >> 3) * (K / 16) * 128 + (k & 15) + (k >> 4) * 128;
-}
 
 // Byte offset of (column n, position k) in the probability operand [p1 | p2]:
 // MN-major, no swizzle.  A core matrix is 8 positions x 16 columns (one
@@ -314,25 +109,6 @@ constexpr uint32_t kPpMnStride = 128;  // between the p1 and p2 core matrices
 constexpr uint32_t kPpKStride = 256;   // between 8-position groups
 __device__ __forceinline__ uint32_t pp_off(int n, int k) {
     return (n >> 4) * kPpMnStride + (n & 15) + (k & 7) * 16 + (k >> 3) * kPpKStride;
-}
-
-// Transpose-reduce: 16 values per lane across the 32 lanes of a warp.  On
-// return v[0] of lane l holds the reduction of value index l >> 1.
-template <bool kMax>
-__device__ __forceinline__ float warp_transpose_reduce(float (&v)[16], int lane) {
-#pragma unroll
-    for (int w = 8, sh = 16; w >= 1; w >>= 1, sh >>= 1) {
-        const bool hi = (lane & sh) != 0;
-#pragma unroll
-        for (int i = 0; i < w; ++i) {
-            const float send = hi ? v[i] : v[i + w];
-            const float keep = hi ? v[i + w] : v[i];
-            const float recv = __shfl_xor_sync(0xffffffffu, send, sh);
-            v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
-        }
-    }
-    const float other = __shfl_xor_sync(0xffffffffu, v[0], 1);
-    return kMax ? fmaxf(v[0], other) : v[0] + other;
 }
 
 // Two probabilities (times 256) -> e4m3 codes of p1 and of 16 * (value - p1),
@@ -999,6 +775,9 @@ cudaError_t encode_cache_maps(CUtensorMap* map3, CUtensorMap* map2, const uint8_
 
 }  // namespace
 
+cudaError_t launch_tc_wide(const DecodeParams& p, const CUtensorMap& map, const CUtensorMap& map_box,
+                           cudaStream_t stream);
+
 // Failure-detection tests only (mla_test_stall_copies): launches issue no page
 // copies, so every wait for a page runs out.
 std::atomic<int> g_test_stall_copies{0};
@@ -1048,8 +827,18 @@ cudaError_t launch_tc_decode(const DecodeParams& p, cudaStream_t stream, bool* h
         map_pages = p.num_pages;
     }
     const int HT = p.H * p.T;
-    // G CTAs (16 rows each) per (partition, request), adjacent in the grid
-    const unsigned G = HT <= kNq ? 1u : static_cast<unsigned>((HT + kNq - 1) / kNq);
+    DecodeParams q = p;
+    q.test_stall_copies = g_test_stall_copies.load();
+    if (HT > kNq) {
+        // More than 16 rows: the wide kernel, ceil(H*T / 32) CTAs per
+        // (partition, request) with the rows shared evenly.
+        q.row_ctas = (HT + kWideRows - 1) / kWideRows;
+        q.rows_per_cta = (HT + q.row_ctas - 1) / q.row_ctas;
+        e = launch_tc_wide(q, map, map_box, stream);
+        if (e == cudaSuccess) *handled = true;
+        return e;
+    }
+    const unsigned G = 1u;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(G * static_cast<unsigned>(p.n_splits), static_cast<unsigned>(p.B));
     cfg.blockDim = dim3(kThreads);
@@ -1063,8 +852,6 @@ cudaError_t launch_tc_decode(const DecodeParams& p, cudaStream_t stream, bool* h
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    DecodeParams q = p;
-    q.test_stall_copies = g_test_stall_copies.load();
     e = HT <= 12 ? cudaLaunchKernelEx(&cfg, tc_decode_kernel<12>, map, map_box, q)
                  : cudaLaunchKernelEx(&cfg, tc_decode_kernel<16>, map, map_box, q);
     if (e != cudaSuccess) return e;

@@ -61,8 +61,8 @@ def test_auto_splits(L, B, max_pages, sm, expect):
 
 
 @pytest.mark.parametrize("B,T,H,max_pages,sm,expect", [
-    (32, 1, 96, 278, 152, 3),      # 96 rows: 6 CTAs per unit, wave cost model
-    (16, 4, 12, 1568, 152, 10),    # 48 rows over mixed lengths: the 160-page cap
+    (32, 1, 96, 278, 152, 3),      # 96 rows: 3 wide CTAs per unit, wave cost model (288 CTAs)
+    (16, 4, 12, 1568, 152, 14),    # 48 rows: 2 wide CTAs per unit, wave cost model (448 CTAs)
     (128, 1, 12, 2219, 152, 14),   # many requests of mixed length: the 160-page cap
     (8, 1, 12, 512, 152, 19),      # one wave, as before
 ])
