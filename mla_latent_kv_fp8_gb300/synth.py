@@ -171,15 +171,17 @@ class ShardedCase:
     shard_len: int
 
 
-def make_sharded_case(seed, B, H, total_len, n_shards, *, device="cpu", with_full=True):
+def make_sharded_case(seed, B, H, total_len, n_shards, *, device="cpu", with_full=True, T=1):
     """Global history of ``total_len`` positions per request, one per-tensor scale
-    over all of it, cut into ``n_shards`` contiguous shards of equal length."""
+    over all of it, cut into ``n_shards`` contiguous shards of equal length.  With
+    T > 1 the last T positions of the history are the draft positions of a
+    multi-token verify (they fall in the last shard)."""
     device = torch.device(device)
     assert total_len % n_shards == 0
     sl = total_len // n_shards
     padded_full = [((total_len + PAGE - 1) // PAGE) * PAGE] * B
     blocks, scale = _latent_codes(seed, padded_full, device)
-    q = make_q(seed, B, 1, H, device)
+    q = make_q(seed, B, T, H, device)
     ks = torch.tensor([scale], dtype=torch.float32, device=device)
     shards = []
     spad = ((sl + PAGE - 1) // PAGE) * PAGE

@@ -60,6 +60,13 @@ def load(path: str | None = None):
         lib.oracle_mla_decode.restype = ctypes.c_int
         lib.oracle_lse_merge.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int, P, P, P, P]
         lib.oracle_lse_merge.restype = ctypes.c_int
+        lib.oracle_e4m3fn_encode.argtypes = [ctypes.c_float]
+        lib.oracle_e4m3fn_encode.restype = ctypes.c_uint8
+        lib.oracle_e4m3fn_encode_array.argtypes = [P, ctypes.c_int64, P]
+        lib.oracle_e4m3fn_encode_array.restype = None
+        lib.oracle_append_latent.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_float, P,
+                                             ctypes.c_int64, ctypes.c_int, P, P, ctypes.c_int64]
+        lib.oracle_append_latent.restype = ctypes.c_int
         if path is None:
             _lib = lib
         return lib
@@ -152,3 +159,40 @@ def merge(part_out, part_lse, *, lib=None):
     if rc != 0:
         raise ValueError(f"oracle_lse_merge failed with code {rc}")
     return out, lse
+
+
+def e4m3fn_encode(x, *, lib=None):
+    """E4M3FN codes of binary32 values: clamp to +-448, round to nearest even,
+    sign kept (NaN -> 0x7F).  Returns a uint8 array of x's shape."""
+    lib = lib or load()
+    xn = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    out = np.zeros(xn.shape, dtype=np.uint8)
+    lib.oracle_e4m3fn_encode_array(xn.ctypes.data, xn.size, out.ctypes.data)
+    return out
+
+
+def append_latent(latent, kv_scale, block_table, start_pos, kv_cache, *, lib=None):
+    """Append new latents to a copy of the paged cache and return it.
+
+    latent: bf16 [B,T,576]; kv_scale: fp32 scalar; block_table int32 [B,max_pages];
+    start_pos int32 [B] (position of latent[b,0] in request b's history);
+    kv_cache uint8 [num_pages,64,576].  Position p = start_pos[b] + t gets the codes
+    e4m3fn(latent[b,t,d] / kv_scale) (binary32 division) in page block_table[b][p//64],
+    row p % 64.  Returns (new_cache uint8 array, status): status -2 if a row was
+    skipped because its position or page id is out of range.
+    """
+    lib = lib or load()
+    ln = _np(latent, np.int16)
+    B, T, d = ln.shape
+    assert d == D_QK
+    btn = _np(block_table, np.int32)
+    spn = _np(start_pos, np.int32)
+    assert btn.shape[0] == B and spn.shape == (B,)
+    kv = _np(kv_cache, np.uint8).copy()
+    assert kv.ndim == 3 and kv.shape[1:] == (PAGE, D_QK)
+    scale = float(_np(kv_scale, np.float32).reshape(-1)[0])
+    rc = lib.oracle_append_latent(ln.ctypes.data, B, T, scale, btn.ctypes.data, btn.shape[1],
+                                  btn.shape[1], spn.ctypes.data, kv.ctypes.data, kv.shape[0])
+    if rc == -1:
+        raise ValueError("oracle_append_latent: bad arguments")
+    return kv, rc

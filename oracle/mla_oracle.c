@@ -384,3 +384,88 @@ int oracle_lse_merge(int S, int64_t rows, int D, const double *part_out,
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------ */
+/* Appending new positions to the cache                                 */
+/* ------------------------------------------------------------------ */
+
+/* Encode a binary32 value as an E4M3FN byte, written out from the format
+ * definition above: magnitudes of 448 and more (the largest finite value)
+ * take 448; otherwise the nearest of the 127 non-negative finite values is
+ * chosen, a tie going to the code whose mantissa is even; the sign bit is the
+ * input's (so -0 and small negative values encode as 0x80).  NaN encodes as
+ * 0x7F. */
+uint8_t oracle_e4m3fn_encode(float x)
+{
+    if (isnan(x))
+        return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (a >= 448.0)
+        return sign | 0x7E;
+    /* the non-negative finite codes 0x00..0x7E have increasing values */
+    int c = 0;
+    while (c + 1 <= 0x7E && oracle_e4m3fn_to_double((uint8_t)(c + 1)) <= a)
+        ++c;
+    double lo = oracle_e4m3fn_to_double((uint8_t)c);
+    if (lo == a)
+        return sign | (uint8_t)c;
+    double hi = oracle_e4m3fn_to_double((uint8_t)(c + 1));
+    double dl = a - lo, dh = hi - a;
+    int pick;
+    if (dl < dh)
+        pick = c;
+    else if (dh < dl)
+        pick = c + 1;
+    else
+        pick = (c & 1) == 0 ? c : c + 1;  /* tie: even mantissa */
+    return sign | (uint8_t)pick;
+}
+
+void oracle_e4m3fn_encode_array(const float *x, int64_t n, uint8_t *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = oracle_e4m3fn_encode(x[i]);
+}
+
+/* The step before the decode in every decode step (the post's model section:
+ * the compressed history grows by one latent per new position): the new
+ * latent of request b at draft position t -- 576 bf16 values, the 512 latent
+ * dims followed by the 64 rotated positional dims -- is divided by kv_scale
+ * in binary32 (one correctly rounded division per value), encoded as E4M3FN
+ * and written to page block_table[b][p / 64], row p % 64, with
+ * p = start_pos[b] + t.  Nothing else in the cache changes.  A row whose
+ * position lies outside [0, max_pages * 64) or whose page id lies outside
+ * [0, num_pages) is not written, and the call returns -2. */
+int oracle_append_latent(const uint16_t *latent, int B, int T, float kv_scale,
+                         const int32_t *block_table, int64_t bt_stride, int max_pages,
+                         const int32_t *start_pos, uint8_t *kv, int64_t num_pages)
+{
+    if (B < 0 || T < 0 || (B > 0 && T > 0 && (!latent || !block_table || !start_pos || !kv)))
+        return -1;
+    int rc = 0;
+    for (int b = 0; b < B; ++b) {
+        for (int t = 0; t < T; ++t) {
+            int64_t p = (int64_t)start_pos[b] + t;
+            if (p < 0 || p >= (int64_t)max_pages * ORACLE_PAGE) {
+                rc = -2;
+                continue;
+            }
+            int32_t page = block_table[(int64_t)b * bt_stride + p / ORACLE_PAGE];
+            if (page < 0 || page >= num_pages) {
+                rc = -2;
+                continue;
+            }
+            uint8_t *dst = kv + ((int64_t)page * ORACLE_PAGE + p % ORACLE_PAGE) * ORACLE_DQK;
+            const uint16_t *src = latent + ((int64_t)b * T + t) * ORACLE_DQK;
+            for (int d = 0; d < ORACLE_DQK; ++d) {
+                uint32_t u = (uint32_t)src[d] << 16;
+                float f;
+                memcpy(&f, &u, sizeof f);
+                float v = f / kv_scale;
+                dst[d] = oracle_e4m3fn_encode(v);
+            }
+        }
+    }
+    return rc;
+}

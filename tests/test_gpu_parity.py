@@ -176,6 +176,35 @@ def test_dcp_shards_merge_to_unsharded(L, impl):
     assert_parity(out, lse, ro, rl, what="merged shards vs unsharded")
 
 
+def test_dcp_verify_shards_merge_to_unsharded(L, impl):
+    """Multi-token verify through the DCP path (section 1): 4 contiguous shards of
+    one history with T = 4 draft positions at its end.  Shards before the last
+    are decoded as T = 1 calls with T*H rows (every draft query sees all of their
+    positions); the last shard keeps T = 4 and the causal rule.  mla_merge_partials
+    of the four (out, lse) equals the unsharded causal oracle."""
+    T, H, n = 4, 12, 4
+    sc = synth.make_sharded_case(19, 3, H, 4 * 700, n, T=T)
+    outs, lses = [], []
+    for s, sh in enumerate(sc.shards):
+        g = sh.to("cuda")
+        B = g.q.shape[0]
+        if s < n - 1:
+            g.q = g.q.reshape(B, 1, T * H, 576)
+            o, l = supported(L, impl, g, 0)
+            o, l = o.reshape(B, T, H, 512), l.reshape(B, T, H)
+        else:
+            o, l = supported(L, impl, g, 0)
+        outs.append(o)
+        lses.append(l)
+    po, pl = torch.stack(outs), torch.stack(lses)
+    out = torch.full(po.shape[1:], float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full(pl.shape[1:], float("nan"), dtype=torch.float32, device="cuda")
+    L.mla_merge_partials(po, pl, n, out, lse)
+    torch.cuda.synchronize()
+    ro, rl = oracle_full(sc.full)
+    assert_parity(out, lse, ro, rl, what="DCP verify: merged shards vs unsharded causal")
+
+
 # ----------------------------------------------------------------------------
 # mla_merge_partials on its own
 # ----------------------------------------------------------------------------

@@ -13,7 +13,7 @@ import torch
 
 import oracle
 from mla_latent_kv_fp8_gb300 import synth
-from tests.test_oracle_pins import _bruteforce
+from tests.test_oracle_pins import _append_case, _bruteforce, _torch_encode
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "mla_oracle.c")
 
@@ -33,6 +33,12 @@ MUTANTS = {
                          "score[(int64_t)h * n + cnt] = acc;"),
     "block_table_row": ("J->block_table[(int64_t)b * J->bt_stride + p / ORACLE_PAGE]",
                         "J->block_table[(int64_t)b + (p / ORACLE_PAGE) * J->bt_stride]"),
+    "encode_tie_away_from_even": ("pick = (c & 1) == 0 ? c : c + 1;", "pick = c + 1;"),
+    "encode_overflow_to_nan": ("if (a >= 448.0)\n        return sign | 0x7E;",
+                               "if (a >= 448.0)\n        return sign | 0x7F;"),
+    "append_row_index": ("kv + ((int64_t)page * ORACLE_PAGE + p % ORACLE_PAGE) * ORACLE_DQK;",
+                         "kv + ((int64_t)page * ORACLE_PAGE + (p + 1) % ORACLE_PAGE) * ORACLE_DQK;"),
+    "append_scale_multiplies": ("float v = f / kv_scale;", "float v = f * kv_scale;"),
 }
 
 
@@ -74,7 +80,14 @@ def _battery(lib):
     mo, ml = oracle.merge(np.stack(po), np.stack(pl), lib=lib)
     if np.abs(mo - wo).max() > 1e-12 * np.abs(wo).max() or np.abs(ml - wl).max() > 1e-12 * np.abs(wl).max():
         return False
-    return True
+    # E4M3FN encoding vs torch's quantiser, and the placement of appended rows
+    rng = np.random.default_rng(3)
+    v = np.r_[rng.standard_normal(4000) * np.exp(rng.uniform(-12, 7, 4000)),
+              np.linspace(440, 500, 121), [17.0, 19.0, 1.0625, 2.0 ** -10]].astype(np.float32)
+    if not np.array_equal(oracle.e4m3fn_encode(v, lib=lib), _torch_encode(v)):
+        return False
+    new, expect, _ = _append_case(lib)
+    return bool(np.array_equal(new, expect))
 
 
 @pytest.fixture(scope="module")

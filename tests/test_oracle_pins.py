@@ -222,6 +222,38 @@ def test_causal_verify_equals_single_token_decodes():
     assert not np.array_equal(l4[:, 0], l4[:, 3])
 
 
+def test_dcp_verify_decomposition_equals_unsharded():
+    """Multi-token verify over a history cut into contiguous DCP shards (post,
+    section 1): every shard but the last holds only positions that all T draft
+    queries see, so it is a T = 1 decode of T*H independent rows; the last shard
+    holds the T draft positions and keeps the causal rule.  Merging the shards'
+    (out, lse) equals the unsharded causal verify."""
+    T, H, n = 4, 3, 4
+    sc = synth.make_sharded_case(17, 2, H, 4 * 96, n, T=T)
+    outs, lses = [], []
+    for s, sh in enumerate(sc.shards):
+        B = sh.q.shape[0]
+        if s < n - 1:
+            q1 = sh.q.reshape(B, 1, T * H, 576).contiguous()
+            o, l = oracle.decode(q1, sh.kv_cache, sh.kv_scale, sh.block_table, sh.seq_lens, sh.sm_scale)
+            o, l = o.reshape(B, T, H, 512), l.reshape(B, T, H)
+        else:
+            o, l = oracle.decode(sh.q, sh.kv_cache, sh.kv_scale, sh.block_table, sh.seq_lens, sh.sm_scale)
+        outs.append(o)
+        lses.append(l)
+    mo, ml = oracle.merge(np.stack(outs), np.stack(lses))
+    ro, rl = oracle.decode(sc.full.q, sc.full.kv_cache, sc.full.kv_scale, sc.full.block_table,
+                           sc.full.seq_lens, sc.full.sm_scale)
+    np.testing.assert_allclose(mo, ro, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(ml, rl, rtol=1e-12, atol=1e-12)
+    # the causal rule inside the last shard matters: treating it as T = 1 differs
+    last = sc.shards[-1]
+    q1 = last.q.reshape(2, 1, T * H, 576).contiguous()
+    _, l_wrong = oracle.decode(q1, last.kv_cache, last.kv_scale, last.block_table, last.seq_lens,
+                               last.sm_scale)
+    assert not np.allclose(l_wrong.reshape(2, T, H), lses[-1])
+
+
 def test_permuted_block_table_equals_identity_layout():
     lens = [300, 64, 1]
     case = synth.make_decode_case(41, lens, 2, 1, extra_pages=5)
@@ -287,3 +319,87 @@ def test_payload_byte_accounting_matches_post():
         g["per_gpu_mb_dcp8"]
     case = synth.make_decode_case(1, [100, 37], 2, 1)
     assert case.kv_bytes() == 137 * 576
+
+
+# --------------------------------------------------------------------------
+# Latent append: E4M3FN encoding and the paged write
+# --------------------------------------------------------------------------
+
+def _torch_encode(x32):
+    """Independent quantiser: torch's float8_e4m3fn cast (round to nearest even)
+    after clamping to the largest finite magnitude."""
+    return torch.clamp(torch.as_tensor(x32, dtype=torch.float32), -448.0, 448.0).to(
+        torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+@pytest.mark.parametrize("scale", [1.0, 0.0091, 2.0 ** -5, 3.7])
+def test_e4m3fn_encode_matches_torch_cast(scale):
+    bits = np.arange(1 << 16, dtype=np.uint32) << 16
+    x = bits.view(np.float32)
+    x = x[np.isfinite(x)]
+    v = (x / np.float32(scale)).astype(np.float32)  # binary32 division, as the append does
+    assert np.array_equal(oracle.e4m3fn_encode(v), _torch_encode(v))
+
+
+def test_e4m3fn_encode_random_binary32_matches_torch_cast():
+    rng = np.random.default_rng(5)
+    v = (rng.standard_normal(200000) * np.exp(rng.uniform(-12, 7, 200000))).astype(np.float32)
+    assert np.array_equal(oracle.e4m3fn_encode(v), _torch_encode(v))
+
+
+def test_e4m3fn_encode_round_trips_every_finite_code():
+    codes = [c for c in range(256) if c not in (0x7F, 0xFF)]
+    vals = np.array([oracle.e4m3fn_to_double(c) for c in codes], dtype=np.float32)
+    assert list(oracle.e4m3fn_encode(vals)) == codes
+
+
+@pytest.mark.parametrize("x,code", [
+    (1.0625, 0x38),        # tie between 1 and 1.125: even mantissa (1.0)
+    (17.0, 0x58),          # tie between 16 and 18 -> 16
+    (19.0, 0x5A),          # tie between 18 and 20 -> 20
+    (2.0 ** -10, 0x00),    # tie between 0 and the smallest subnormal -> 0
+    (1.5 * 2.0 ** -9, 0x02),
+    (-2.0 ** -11, 0x80),   # rounds to -0
+    (448.0, 0x7E), (464.0, 0x7E), (1e30, 0x7E), (-1e30, 0xFE),  # saturation
+])
+def test_e4m3fn_encode_ties_and_saturation(x, code):
+    assert int(oracle.e4m3fn_encode(np.array([x], dtype=np.float32))[0]) == code
+
+
+def _append_case(lib=None):
+    """(new cache from the oracle, cache expected from torch's quantiser, old cache)."""
+    rng = np.random.default_rng(9)
+    num_pages, B, T = 12, 3, 3
+    kv = rng.integers(0, 0x7E, size=(num_pages, 64, 576), dtype=np.uint8)
+    bt = rng.permutation(num_pages)[:B * 4].reshape(B, 4).astype(np.int32)
+    start = np.array([62, 0, 190], dtype=np.int32)  # crosses a page boundary; the last page
+    lat = torch.from_numpy(rng.standard_normal((B, T, 576)).astype(np.float32) * 3).to(torch.bfloat16)
+    lat[0, 1, 7] = 5000.0  # saturates
+    scale = np.float32(0.0123)
+    new, rc = oracle.append_latent(lat, torch.tensor([scale]), bt, start, kv, lib=lib)
+    assert rc == 0
+    expect = kv.copy()
+    for b in range(B):
+        for t in range(T):
+            p = int(start[b]) + t
+            v = (lat[b, t].float().numpy() / scale).astype(np.float32)
+            expect[bt[b, p // 64], p % 64] = _torch_encode(v)
+    return new, expect, kv
+
+
+def test_append_writes_exactly_the_new_rows():
+    new, expect, old = _append_case()
+    assert np.array_equal(new, expect)
+    assert not np.array_equal(new, old)
+
+
+def test_append_skips_rows_out_of_range():
+    num_pages = 4
+    kv = np.zeros((num_pages, 64, 576), dtype=np.uint8)
+    bt = np.array([[0, 1], [2, 9]], dtype=np.int32)  # request 1's second page id is out of range
+    lat = torch.ones((2, 2, 576), dtype=torch.bfloat16)
+    new, rc = oracle.append_latent(lat, torch.tensor([1.0]), bt, np.array([127, 63], dtype=np.int32), kv)
+    assert rc == -2
+    assert (new[1, 63] == 0x38).all()           # request 0, position 127: written
+    assert (new[2, 63] == 0x38).all()           # request 1, position 63: written
+    assert int(new.astype(np.int64).sum()) == 2 * 576 * 0x38   # positions 128 / 64 (bad page): skipped
