@@ -46,6 +46,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-ceiling", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-append", action="store_true")
     return ap.parse_args()
 
 
@@ -319,7 +320,8 @@ def run_ours(args):
     # ---- the ceiling of this access pattern: the same pages, no arithmetic ----
     ceiling = None
     if not args.no_ceiling:
-        ceiling = stream_ceiling(L, base, caches, n_copies, B * n_eff * -(-(H * T) // 16), stream)
+        rows_ctas = 1 if H * T <= 16 else -(-(H * T) // 32)  # CTAs per (request, partition)
+        ceiling = stream_ceiling(L, base, caches, n_copies, B * n_eff * rows_ctas, stream)
 
     # ---- end to end through the C ABI with host buffers ----
     e2e = None
@@ -367,6 +369,41 @@ def run_ours(args):
                "device, decode, one copy of out+lse -> pinned host, stream synchronised every "
                "step; the latent cache is resident decode state"}
 
+    # ---- the latent append that precedes each decode step (one call) ----
+    append = None
+    if not args.no_append:
+        lat = synth.make_latent(77, B, T, device=dev)
+        start = (base.seq_lens - T).to(torch.int32)
+        kv_app = caches[-1]  # after the timed regions: rewriting the newest positions is harmless now
+
+        def app():
+            L.mla_append_latent(lat, base.kv_scale, base.block_table, start, kv_app, stream)
+
+        for _ in range(10):
+            app()
+        barrier()
+        gapp = torch.cuda.CUDAGraph()  # as a serving loop launches it: no host cost per call
+        with torch.cuda.graph(gapp, stream=stream):
+            for _ in range(100):
+                app()
+        with torch.cuda.stream(stream):
+            gapp.replay()
+        barrier()
+        napp = 10
+        ev0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(napp):
+                gapp.replay()
+        ev1.record(stream)
+        barrier()
+        assert L.mla_device_error() == 0
+        app_us = ev0.elapsed_time(ev1) * 1e3 / (napp * 100)
+        app_bytes = B * T * (576 * 2 + 576) + B * (4 + 4)
+        append = {"us_per_call": round(app_us, 3), "bytes_per_call": app_bytes,
+                  "gbps": round(app_bytes / (app_us * 1e-6) / 1e9, 2), "positions": B * T,
+                  "note": "mla_append_latent of one new latent per query position (bf16 in, e4m3 out), "
+                          "CUDA-graph replays of 100 calls; launch-bound by size"}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(base, budget_s=15.0)
@@ -394,6 +431,7 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "e2e": e2e,
             "stream_ceiling": ceiling,
+            "append": append,
             "gpu_launches": args.steps * (1 + (1 if n_eff > 1 else 0)),
             "clocks": clocks,
         }

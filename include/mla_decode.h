@@ -165,6 +165,38 @@ mla_status_t mla_decode_paged_noalloc(const mla_tensor_t *q, const mla_tensor_t 
                                       float sm_scale, const mla_tensor_t *out,
                                       const mla_tensor_t *lse, void *stream);
 
+/*
+ * mla_append_latent -- write the new positions of a decode step into the
+ * paged FP8 cache (the post's model section: each layer's compressed history
+ * grows by one latent per new position; section 1: 576 FP8 bytes per
+ * position, no per-position scale).
+ *
+ *   latent      bf16 [B, T, 576], device, contiguous, 16-byte aligned; the new
+ *               latents (512 latent dims, then the 64 rotated positional dims)
+ *               of T new positions per request.
+ *   kv_scale    device pointer to the fp32 per-tensor scale of the cache.
+ *   block_table i32 [B, max_pages], device, rows contiguous (as for decode).
+ *   start_pos   i32 [B], device: position of latent[b, 0] in request b's
+ *               history (its length before the append).
+ *   kv_cache    e4m3fn [num_pages, 64, 576], device, contiguous, 16-byte
+ *               aligned; written in place.
+ *   stream      cudaStream_t as void*.
+ *
+ * Position p = start_pos[b] + t receives code[d] = e4m3fn(latent[b,t,d] /
+ * kv_scale) -- one correctly rounded fp32 division, round to nearest even,
+ * magnitudes beyond 448 saturate to +-448 (NaN stays NaN) -- in page
+ * block_table[b][p / 64], row p % 64.  No other cache byte changes.  A decode
+ * that follows on the same stream with seq_lens[b] = start_pos[b] + T sees
+ * the new positions.  Rows whose position lies outside [0, max_pages * 64)
+ * or whose page id lies outside [0, num_pages) are not written and set the
+ * device error word (3 or 2; see mla_device_error).
+ * Returns MLA_OK or an error status (nothing is launched on error); B*T = 0
+ * is a no-op.  The call allocates nothing and never synchronises.
+ */
+mla_status_t mla_append_latent(const mla_tensor_t *latent, const float *kv_scale,
+                               const mla_tensor_t *block_table, const mla_tensor_t *start_pos,
+                               const mla_tensor_t *kv_cache, void *stream);
+
 /* The automatic split count used when n_splits == 0: enough history
  * partitions per request that B * splits fills every SM of the device
  * (at least one full wave), with at least 2 pages (128 positions) each.

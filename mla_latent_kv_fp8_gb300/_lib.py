@@ -28,7 +28,8 @@ _DTYPES = {torch.bfloat16: 1, torch.float32: 2, torch.uint8: 3, torch.float8_e4m
 EXPORTS = ("mla_decode_paged", "mla_merge_partials", "mla_auto_splits", "mla_split_chunk_pages",
            "mla_decode_workspace_bytes", "mla_set_impl", "mla_device_error", "mla_status_string",
            "mla_last_error", "mla_profile_next_decode", "mla_last_decode_impl",
-           "mla_decode_paged_noalloc", "mla_test_stall_copies", "mla_bench_stream_pages")
+           "mla_decode_paged_noalloc", "mla_test_stall_copies", "mla_bench_stream_pages",
+           "mla_append_latent")
 
 
 class MlaError(RuntimeError):
@@ -54,6 +55,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mla_decode_paged.restype = ctypes.c_int
     lib.mla_decode_paged_noalloc.argtypes = [T, T, P, T, T, ctypes.c_int32, ctypes.c_float, T, T, P]
     lib.mla_decode_paged_noalloc.restype = ctypes.c_int
+    lib.mla_append_latent.argtypes = [T, P, T, T, T, P]
+    lib.mla_append_latent.restype = ctypes.c_int
     lib.mla_merge_partials.argtypes = [T, T, ctypes.c_int32, T, T, P]
     lib.mla_merge_partials.restype = ctypes.c_int
     lib.mla_auto_splits.argtypes = [ctypes.c_int32] * 5
@@ -142,6 +145,14 @@ def mla_decode_paged_noalloc(q, kv_cache, kv_scale, block_table, seq_lens, n_spl
     _check(lib().mla_decode_paged_noalloc(_ref(dq), _ref(dkv), ctypes.c_void_p(kv_scale.data_ptr()),
                                           _ref(dbt), _ref(dsl), int(n_splits), float(sm_scale),
                                           _ref(do), _ref(dl), _stream(stream)))
+
+
+def mla_append_latent(latent, kv_scale, block_table, start_pos, kv_cache, stream=None):
+    """Quantise latent [B, T, 576] (bf16) to e4m3fn(x / kv_scale) and write position
+    start_pos[b] + t of each request into its paged slot of kv_cache, in place."""
+    dl, dbt, dsp, dkv = describe(latent), describe(block_table), describe(start_pos), describe(kv_cache)
+    _check(lib().mla_append_latent(_ref(dl), ctypes.c_void_p(kv_scale.data_ptr()), _ref(dbt), _ref(dsp),
+                                   _ref(dkv), _stream(stream)))
 
 
 def mla_merge_partials(partial_out, partial_lse, n_shards, out, lse=None, stream=None):

@@ -148,6 +148,13 @@ def make_q(seed, B, T, H, device="cpu"):
     return q.to(torch.bfloat16).to(device)
 
 
+def make_latent(seed, B, T, device="cpu", amplitude=1.0):
+    """New latents of T positions per request: bf16 [B, T, 576] ~ amplitude * N(0, 1)."""
+    rng = np.random.default_rng([int(seed), 5])
+    x = rng.standard_normal((B, T, D_QK), dtype=np.float32) * np.float32(amplitude)
+    return torch.from_numpy(x).to(torch.bfloat16).to(device)
+
+
 def make_decode_case(seed, lens, H, T=1, *, device="cpu", permute=True, max_pages=None,
                      extra_pages=0, kv_scale=None, sm_scale=SM_SCALE) -> DecodeCase:
     """Seeded decode inputs for contexts ``lens`` (each includes the T new positions)."""

@@ -178,3 +178,41 @@ def test_stream_probe_rejects_bad_arguments_on_host(L):
     assert lib.mla_bench_stream_pages(ctypes.c_void_p(4096), 1 << 25, ids, 1, 1, None) == 1
     assert lib.mla_bench_stream_pages(ctypes.c_void_p(4096), 8, ids, 0, 1, None) == 1   # no CTAs
     assert lib.mla_bench_stream_pages(ctypes.c_void_p(4096), 8, ids, 1, 0, None) == 1
+
+
+def _call_append(L, lat, bt, sp, kv, scale_ptr=0x20000):
+    ref = lambda d: ctypes.byref(d) if d is not None else None  # noqa: E731
+    return L.lib().mla_append_latent(ref(lat), ctypes.c_void_p(scale_ptr), ref(bt), ref(sp), ref(kv), None)
+
+
+def _good_append(B=2, T=1, mp=4, npages=8):
+    return dict(lat=_desc([B, T, 576], 1), bt=_desc([B, mp], 4), sp=_desc([B], 4), kv=_desc([npages, 64, 576], 3))
+
+
+@pytest.mark.parametrize("mutate,status", [
+    (lambda a: a.update(lat=None), 1),
+    (lambda a: setattr(a["lat"], "dtype", 2), 1),                 # fp32 latents
+    (lambda a: a.update(lat=_desc([2, 1, 512], 1)), 2),           # 512-wide latents
+    (lambda a: a.update(bt=_desc([3, 4], 4)), 1),                 # block table of 3 requests
+    (lambda a: a.update(sp=_desc([3], 4)), 1),                    # start positions of 3 requests
+    (lambda a: a.update(sp=_desc([2], 2)), 1),                    # fp32 start positions
+    (lambda a: a.update(kv=_desc([8, 32, 576], 3)), 2),           # page size 32
+    (lambda a: a.update(kv=_desc([8, 64, 576], 1)), 1),           # bf16 cache
+    (lambda a: setattr(a["lat"], "data", 0x10008), 2),           # misaligned latents
+    (lambda a: a["kv"].stride.__setitem__(1, 1152), 2),          # non-contiguous cache
+])
+def test_append_rejects_bad_arguments_on_host(L, mutate, status):
+    a = _good_append()
+    mutate(a)
+    st = _call_append(L, a["lat"], a["bt"], a["sp"], a["kv"])
+    assert st == status, L.mla_last_error()
+    assert L.mla_last_error() != ""
+
+
+def test_append_null_scale_and_empty_batch(L):
+    a = _good_append()
+    assert _call_append(L, a["lat"], a["bt"], a["sp"], a["kv"], scale_ptr=0) == 1
+    a = _good_append(B=0)
+    assert _call_append(L, a["lat"], a["bt"], a["sp"], a["kv"]) == 0
+    a = _good_append(T=0)
+    assert _call_append(L, a["lat"], a["bt"], a["sp"], a["kv"]) == 0
