@@ -15,19 +15,21 @@
 // adjacent in the grid, share each page through L2.
 //   * QK^T, swap-AB as in the 12-head kernel: D[64 pos x 64] = K_page[64 x 576] .
 //     [q1 | q2]^T with the exact two-term e4m3 split of the query
-//     (q * 2^e = q1 + q2 / 16): 18 MMAs of N = 64 per page, issued by two
-//     warps (even and odd pages) because one thread needs ~40 cycles per MMA.
+//     (q * 2^e = q1 + q2 / 16).  One thread needs ~40 cycles to issue a
+//     tcgen05.mma, so the 18 MMAs of a page are split along K between two
+//     warps, each accumulating its half of the dims into its own 64 columns;
+//     the attention warps add the halves.
 //   * Four attention warpgroups split the ROWS: warpgroup g owns rows
 //     [8g, 8g + 8) of every page, so each row keeps one reference, one
 //     normaliser and one output column pair, and no merge of warpgroups is
 //     needed at the end.  Each lane works on 4 rows of one position.
 //   * PV: D[128 dims x 64] += V^T[128 x 64 pos] . [p1 | p2]^T per 128-dim block,
 //     P = p1 + p2 / 16 in e4m3 (relative error ~2^-8), 8 MMAs of N = 64 per page.
-//   * TMEM: 4 score buffers x 64 columns + output 4 blocks x 64 columns = 512.
+//   * TMEM: 2 score tiles x 128 columns + output 4 blocks x 64 columns = 512.
 // Warp roles (640 threads, one CTA per SM): warp 0 TMA producer (ring of 4
 // pages), warps 1 and 3 issue QK^T, warp 2 issues PV, warps 4-19 are the four
-// attention warpgroups.  Every wait is bounded; on timeout the kernel records
-// an error, drains its copies and MMAs, frees TMEM and returns.
+// attention warpgroups.  Every wait is bounded; on timeout the kernel
+// records an error, drains its copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -42,14 +44,14 @@
 namespace mla {
 namespace {
 
-constexpr int kWThreads = 640;
+constexpr int kWThreads = 640;               // 20 warps
 constexpr int kWGroups = 4;                  // attention warpgroups
 constexpr int kWRows = 32;                   // rows (t, h) per CTA
 constexpr int kWRg = kWRows / kWGroups;      // 8 rows per warpgroup
 constexpr int kWRL = kWRg / 2;               // 4 rows per lane
 constexpr int kWN = 2 * kWRows;              // MMA N: q1 | q2 rows (QK), p1 | p2 rows (PV)
 constexpr int kWStages = 4;                  // page slots in the TMA ring
-constexpr int kWSBufs = 4;                   // score tiles in TMEM
+constexpr int kWSBufs = 2;                   // score tiles in TMEM, each two K-halves of 64 columns
 constexpr int kWPBufs = 4;                   // probability operands in shared memory
 constexpr int kWSlotBytes = kPage * kDqk;    // 36,864: one page
 constexpr int kWBoxBytes = kPage * 64;       // 4,096: 64 positions x 64 dims
@@ -58,11 +60,17 @@ constexpr int kWQpBytes = kWN * kDqk;        // 36,864
 constexpr int kWPpKStride = kWN / 16 * 128;  // 512: bytes between 8-position groups of P
 constexpr int kWPpBytes = kWN * kPage;       // 4,096
 constexpr uint32_t kWTmemCols = 512;
-constexpr uint32_t kWOCol0 = kWSBufs * kWN;  // 256: output tile, block c at + 64 c
+constexpr uint32_t kWSCols = 2 * kWN;        // 128: one score tile (K-half a | K-half b)
+constexpr uint32_t kWOCol0 = kWSBufs * kWSCols;  // 256: output tile, block c at + 64 c
 constexpr int kWSetupBar = 1 + kWGroups;     // named barrier of the set-up (warps 1..19)
 constexpr float kWHeadroom = 8.f;            // log2 units a score may exceed its row's reference
 constexpr float kWShift = 4.f;               // a new reference sits this far below the page max
 static_assert(kWOCol0 + 4 * kWN <= kWTmemCols, "TMEM budget");
+// The probabilities of page i go to buffer i % kWPBufs, last read by the PV of
+// page i - kWPBufs.  With as many buffers as ring slots that PV has finished
+// before the scores of page i exist: page i was copied into the slot that PV
+// released, and QK^T of page i waited for the copy.
+static_assert(kWPBufs == kWStages, "probability buffers are freed through the page ring");
 
 struct WideSmem {
     uint8_t slot[kWStages][kWSlotBytes];     // 1024-aligned page tiles (64-byte swizzle)
@@ -100,6 +108,13 @@ __device__ __forceinline__ void wsplit_p(float a0, float a1, uint32_t& c1, uint3
     const __half2 r = __hmul2(__hsub2(h, *reinterpret_cast<const __half2*>(&br)), __float2half2_rn(16.f));
     c2 = static_cast<uint32_t>(
         __nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&r), __NV_SATFINITE, __NV_E4M3));
+}
+
+// 2^x with the special function unit (inputs here lie in [-inf, 8]).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 // Sum of 8 values per lane across the warp: on return lane l holds the sum of
@@ -212,7 +227,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
             mbar_init(&S.empty[s], 1);
         }
         for (int i = 0; i < kWSBufs; ++i) {
-            mbar_init(&S.s_full[i], 1);
+            mbar_init(&S.s_full[i], 2);              // both K-halves of QK^T
             mbar_init(&S.s_empty[i], 4 * kWGroups);  // every attention warp reads every score tile
         }
         for (int i = 0; i < kWPBufs; ++i) {
@@ -352,28 +367,31 @@ __global__ void __launch_bounds__(kWThreads, 1)
         }
     } else if (warp == 1 || warp == 3) {
         // ======================= QK^T issuers =======================
-        // Warp 1 issues the even pages, warp 3 the odd ones; the whole warp runs
-        // the loop, one elected lane issues.
+        // Both warps take every page: warp 1 the K-steps over dims [0, 288) into
+        // the first half of the score tile, warp 3 those over [288, 576) into the
+        // second half (one thread needs ~40 cycles per MMA, so the split halves
+        // the time to the page's scores).  The whole warp runs the loop, one
+        // elected lane issues.  Pages are taken in order, so the parity of a
+        // slot's full barrier is exact.
         const int me = warp == 1 ? 0 : 1;
         const bool leader = elect_one();
         const uint64_t qd = smem_desc(smem_u32(S.qp), 128, (kDqk / 16) * 128, kLayoutNone);
         constexpr uint32_t kIdesc = idesc_e4m3(64, kWN, false, false);
-        for (int i = me; i < n_pages; i += 2) {
+        constexpr int kHalf = kDqk / 64;  // 9 K-steps of 32 dims per issuer
+        for (int i = 0; i < n_pages; ++i) {
             const int s = i % kWStages, sb = i % kWSBufs;
-            // Slot s last held page i - kWStages: wait for its PV (which also
-            // gates the copy of page i) so that the parity test of full[s]
-            // cannot match a phase two behind.
-            if (i >= kWStages && !warp_wait(&S.empty[s], ((i / kWStages) & 1) ^ 1, abort, p.err)) break;
             if (!warp_wait(&S.full[s], (i / kWStages) & 1, abort, p.err)) break;
             if (!warp_wait(&S.s_empty[sb], ((i / kWSBufs) & 1) ^ 1, abort, p.err)) break;
             tc_fence_after();
             const uint64_t ad = smem_desc(smem_u32(S.slot[s]), 16, 512, kLayoutSw64);
-            const uint32_t d = tmem + kWN * sb;
+            const uint32_t d = tmem + kWSCols * sb + kWN * me;
             if (leader) {
 #pragma unroll
-                for (int ks = 0; ks < kDqk / 32; ++ks)
+                for (int j = 0; j < kHalf; ++j) {
+                    const int ks = kHalf * me + j;
                     mma_e4m3(d, ad + static_cast<uint64_t>(((ks >> 1) * kWBoxBytes + (ks & 1) * 32) >> 4),
-                             qd + static_cast<uint64_t>(ks * 16), kIdesc, ks > 0);
+                             qd + static_cast<uint64_t>(ks * 16), kIdesc, j > 0);
+                }
                 mma_commit(&S.s_full[sb]);
             }
             __syncwarp();
@@ -468,11 +486,18 @@ __global__ void __launch_bounds__(kWThreads, 1)
             if (!fail) fail = !warp_wait(&S.s_full[sb], (i / kWSBufs) & 1, abort, p.err);
             if (!fail) {
                 tc_fence_after();
-                uint32_t r1[8], r2[8];
-                const uint32_t ta = tmem + lane_base + kWN * sb + kWRg * g;
-                tmem_ld8(ta, r1);            // q1 . x of the group's rows
-                tmem_ld8(ta + kWRows, r2);   // q2 . x
+                uint32_t r1[8], r2[8], r1b[8], r2b[8];
+                const uint32_t ta = tmem + lane_base + kWSCols * sb + kWRg * g;
+                tmem_ld8(ta, r1);                   // q1 . x over dims [0, 288) of the group's rows
+                tmem_ld8(ta + kWRows, r2);          // q2 . x
+                tmem_ld8(ta + kWN, r1b);            // the same over dims [288, 576)
+                tmem_ld8(ta + kWN + kWRows, r2b);
                 tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    r1[j] = __float_as_uint(__uint_as_float(r1[j]) + __uint_as_float(r1b[j]));
+                    r2[j] = __float_as_uint(__uint_as_float(r2[j]) + __uint_as_float(r2b[j]));
+                }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&S.s_empty[sb]);
@@ -548,12 +573,11 @@ __global__ void __launch_bounds__(kWThreads, 1)
                 }
             }
             // ---- probabilities of this page -> this group's rows of [p1 | p2] ----
-            // Buffer kb was last read by the PV of page i - kWPBufs.
-            if (!fail && i >= kWPBufs) fail = !warp_wait(&S.pv_done[kb], ((i / kWPBufs) - 1) & 1, abort, p.err);
+            // (buffer kb is free: see the static_assert on kWPBufs)
             if (!fail) {
 #pragma unroll
                 for (int j = 0; j < kWRL; ++j) {
-                    s[j] = (s[j] == NEG) ? 0.f : exp2f(s[j] - rr[j]);
+                    s[j] = (s[j] == NEG) ? 0.f : fast_exp2(s[j] - rr[j]);
                     lp[j] += s[j];
                 }
                 uint32_t c1a, c2a, c1b, c2b;
