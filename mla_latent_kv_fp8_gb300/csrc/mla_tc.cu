@@ -1,5 +1,7 @@
 // mla_tc.cu -- tcgen05 tensor-core split-KV MLA decode over a paged FP8 latent
-// cache, for sm_103a (GB300).
+// cache, for sm_103a (GB300): the kernel for units of up to 16 query rows
+// (H * T <= 16, e.g. 12 heads x 1 position), and the dispatch to the wide
+// kernel (mla_tc_wide.cu) for 17..128 rows.
 //
 // Method: "Kimi K3 on AMD Instinct MI355X" post -- section 4 (the history is
 // cut into parallel partitions inside one GPU and the partial results are
@@ -137,15 +139,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Launched as a programmatic dependent of the previous kernel on the stream:
     // everything before this point overlaps its tail; nothing is read before it.
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    // More than 16 rows: G = ceil(H*T / 16) CTAs per (partition, request), CTA
-    // r taking rows [16r, 16r + 16) of every page.  They are adjacent in the
-    // grid, so they run at the same time and all but the first read each page
-    // from L2 (HBM still sees each page about once).
-    const int G = HT > kNq ? (HT + kNq - 1) / kNq : 1;
-    const int crank = G > 1 ? static_cast<int>(blockIdx.x % G) : 0;
-    const int split = blockIdx.x / G, b = blockIdx.y;
-    const int r0 = kNq * crank;                  // first (t, h) row of this CTA
-    const int HTc = min(kNq, HT - r0);           // rows of this CTA
+    // One CTA per (partition, request) with all of its H*T <= 16 rows (units
+    // of more rows run on the wide kernel).
+    const int split = blockIdx.x, b = blockIdx.y;
+    const int HTc = HT;                          // rows of this CTA
     volatile int* abort = &S.abort;
 
     // Global loads that depend only on the launch indices go out together,
@@ -166,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int rr = 0; rr < 2; ++rr) {
             const int r = warp - 1 + (kThreads / 32 - 1) * rr;
-            const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)b * HT + r0 + r) * kDqk);
+            const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)b * HT + r) * kDqk);
 #pragma unroll
             for (int k = 0; k < 3; ++k) {
                 const int c = lane + 32 * k;  // 16-byte chunk: 8 bf16 values
@@ -187,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // None of this request's history falls in this partition: leave before
         // any set-up.  Its rows get lse = -inf, a partial the merge skips, or,
         // unsplit, out = 0 and lse = -inf.
-        const int64_t row0 = (int64_t)b * HT + r0;
+        const int64_t row0 = (int64_t)b * HT;
         if (p.n_splits == 1) {
             for (int idx = tid; idx < HTc * kDv; idx += kThreads) p.out[row0 * kDv + idx] = 0;
             if (p.lse)
@@ -232,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto issue_page = [&](int i, int32_t pid) {
         const int s = i % kStages;
         if (pid < 0 || pid >= p.num_pages) {
-            if (crank == 0) atomicCAS(p.err, 0, kErrPageRange);
+            atomicCAS(p.err, 0, kErrPageRange);
             pid = 0;  // load a valid page; the softmax masks and zeroes it
         }
         mbar_expect_tx(&S.full[s], kSlotBytes);
@@ -303,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (lane == 0) {
                 S.row_scale[r] = kv_scale * p.sm_scale_log2 * ldexpf(1.f, -e);
-                S.rowlim[r] = (L == 0) ? 0 : L - p.T + 1 + (r0 + r) / p.H;
+                S.rowlim[r] = (L == 0) ? 0 : L - p.T + 1 + r / p.H;
             }
         } else {
             for (int c = lane; c < kDqk / 8; c += 32) {
@@ -678,7 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 w_park *= inv;
                 if (quad == 0 && lane < HTc) {
                     const float lse = (l > 0.f) ? (mn + log2f(l)) * kLn2 : -INFINITY;
-                    const int64_t grow = (int64_t)b * HT + r0 + lane;
+                    const int64_t grow = (int64_t)b * HT + lane;
                     if (direct) {
                         if (p.lse) p.lse[grow] = lse;
                     } else {
@@ -694,7 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < 4; ++c) o[c][h] = fmaf(tile[h * kDv + 128 * c + d], wp, o[c][h] * wo);
             }
-            const int64_t row0 = (int64_t)b * HT + r0;  // this CTA's first answer row
+            const int64_t row0 = (int64_t)b * HT;  // this CTA's first answer row
 #pragma unroll
             for (int h = 0; h < kRows; ++h) {
                 if (h < HTc) {
@@ -838,9 +835,8 @@ cudaError_t launch_tc_decode(const DecodeParams& p, cudaStream_t stream, bool* h
         if (e == cudaSuccess) *handled = true;
         return e;
     }
-    const unsigned G = 1u;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(G * static_cast<unsigned>(p.n_splits), static_cast<unsigned>(p.B));
+    cfg.gridDim = dim3(static_cast<unsigned>(p.n_splits), static_cast<unsigned>(p.B));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = sizeof(Smem) + 1024;
     cfg.stream = stream;

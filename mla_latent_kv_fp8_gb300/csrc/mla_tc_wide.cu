@@ -68,9 +68,10 @@ constexpr float kWShift = 4.f;               // a new reference sits this far be
 static_assert(kWOCol0 + 4 * kWN <= kWTmemCols, "TMEM budget");
 // The probabilities of page i go to buffer i % kWPBufs, last read by the PV of
 // page i - kWPBufs.  With as many buffers as ring slots that PV has finished
-// before the scores of page i exist: page i was copied into the slot that PV
-// released, and QK^T of page i waited for the copy.
-static_assert(kWPBufs == kWStages, "probability buffers are freed through the page ring");
+// before the scores of page i exist (page i was copied into the slot that PV
+// released, and QK^T of page i waited for the copy), so no wait is needed;
+// with fewer buffers the attention warps wait for it.
+static_assert(kWPBufs <= kWStages, "probability buffers");
 
 struct WideSmem {
     uint8_t slot[kWStages][kWSlotBytes];     // 1024-aligned page tiles (64-byte swizzle)
@@ -573,7 +574,10 @@ __global__ void __launch_bounds__(kWThreads, 1)
                 }
             }
             // ---- probabilities of this page -> this group's rows of [p1 | p2] ----
-            // (buffer kb is free: see the static_assert on kWPBufs)
+            if constexpr (kWPBufs < kWStages) {
+                if (!fail && i >= kWPBufs)
+                    fail = !warp_wait(&S.pv_done[kb], ((i / kWPBufs) - 1) & 1, abort, p.err);
+            }
             if (!fail) {
 #pragma unroll
                 for (int j = 0; j < kWRL; ++j) {

@@ -103,7 +103,10 @@ def test_reduced_workloads_match_oracle(L, impl, name, n_splits):
 @pytest.mark.parametrize("lens,H,T", [
     ([1], 12, 1), ([64], 12, 1), ([65], 12, 1), ([128, 129, 127], 12, 1), ([4, 5, 68], 12, 4),
     ([0, 300, 0], 12, 1), ([200], 1, 1), ([333, 17], 7, 3), ([260], 128, 1), ([190, 66], 32, 4),
-    ([517], 16, 8), ([1000], 96, 1), ([300, 77], 14, 1), ([260, 9], 4, 4), ([700], 16, 1)])
+    ([517], 16, 8), ([1000], 96, 1), ([300, 77], 14, 1), ([260, 9], 4, 4), ([700], 16, 1),
+    # the wide kernel at its boundaries: 17 rows (1 CTA), 33 (2 CTAs of 17 + 16),
+    # 65 (3 CTAs), 100 and 120 (4 CTAs), causal with 6 and 13 draft positions
+    ([70, 1, 0], 17, 1), ([200, 129], 33, 1), ([640, 64], 5, 13), ([129], 100, 1), ([300], 20, 6)])
 def test_edge_shapes_match_oracle(L, impl, lens, H, T):
     case = synth.make_decode_case(1000 + sum(lens) + H + T, lens, H, T, extra_pages=3)
     for n_splits in (0, 1, 3):
