@@ -36,8 +36,9 @@
  * Errors: every entry point validates its arguments on the host before any
  * launch and returns a status; mla_last_error() gives a message for the last
  * failing call of the calling thread.  Device kernels never trap: bounded
- * waits and (in bounds-checking builds) index checks write a device error
- * word that mla_device_error() reads.
+ * waits and the checks of device-resident indices (page ids, sequence
+ * lengths, append positions) write a device error word that
+ * mla_device_error() reads.
  */
 #ifndef MLA_DECODE_H_
 #define MLA_DECODE_H_
@@ -111,8 +112,11 @@ typedef enum {
  *
  * Limits: H * T <= 128; dims fixed at 576 / 512; page size fixed at 64.
  * Returns MLA_OK or an error status (nothing is launched on error).
- * Out-of-range page ids and seq_lens are not checked on the host (that would
- * need a synchronisation); bounds-checking builds flag them on the device.
+ * Page ids and seq_lens live on the device, so the host cannot check them
+ * without a synchronisation; the kernels do: a page id outside
+ * [0, num_pages) is not read (its 64 positions contribute nothing) and sets
+ * device error 2; a seq_len outside [0, 64 * max_pages], or in (0, T), is
+ * treated as 0 and sets device error 3 (see mla_device_error).
  */
 mla_status_t mla_decode_paged(const mla_tensor_t *q, const mla_tensor_t *kv_cache,
                               const float *kv_scale, const mla_tensor_t *block_table,

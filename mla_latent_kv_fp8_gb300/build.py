@@ -31,8 +31,6 @@ def _flags(verbose_ptxas: bool):
          "--expt-relaxed-constexpr", *ARCH]
     if verbose_ptxas:
         f += ["-Xptxas", "-v"]
-    if os.environ.get("MLA_BOUNDS_CHECK"):
-        f += ["-DMLA_BOUNDS_CHECK=1"]
     return f
 
 

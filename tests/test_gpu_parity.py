@@ -142,6 +142,42 @@ def test_unread_cache_bytes_do_not_leak(L, impl):
     assert_parity(out, lse, ro, rl, what="garbage outside the visible history")
 
 
+def test_out_of_range_page_id_and_seq_len_are_masked_and_reported(L, impl):
+    """Device-resident indices are checked on the device: a page id out of range
+    is not read (its positions drop out of the softmax) and a seq_len beyond the
+    block table is treated as 0; each sets its device error code."""
+    lens = [300, 200, 90]
+    case = synth.make_decode_case(88, lens, 12, 1, extra_pages=2)
+    bt = case.block_table.clone()
+    bt[1, 1] = case.kv_cache.shape[0] + 7           # request 1, positions 64..127
+    case.block_table = bt
+    B = len(lens)
+    out = torch.full((B, 1, 12, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, 1, 12), float("nan"), device="cuda")
+    g = case.to("cuda")
+    L.mla_decode_paged(g.q, g.kv_cache, g.kv_scale, g.block_table, g.seq_lens, 0, g.sm_scale, out, lse)
+    torch.cuda.synchronize()
+    assert L.mla_device_error() == 2
+    for b in range(B):
+        mask = np.ones(max(lens), dtype=np.uint8)
+        if b == 1:
+            mask[64:128] = 0
+        bt_b = case.block_table[b:b + 1].clone()
+        bt_b[bt_b >= case.kv_cache.shape[0]] = 0    # the oracle reads only kept positions
+        ro, rl = oracle.decode(case.q[b:b + 1], case.kv_cache, case.kv_scale, bt_b,
+                               case.seq_lens[b:b + 1], case.sm_scale, pos_mask=mask)
+        assert_parity(out[b:b + 1], lse[b:b + 1], ro, rl, what=f"request {b} with a bad page id")
+    # a seq_len beyond 64 * max_pages: that request reads nothing
+    sl = case.seq_lens.clone()
+    sl[2] = 64 * case.block_table.shape[1] + 1
+    L.mla_decode_paged(g.q, g.kv_cache, g.kv_scale, case.block_table.cuda(), sl.cuda(), 0, g.sm_scale,
+                       out, lse)
+    torch.cuda.synchronize()
+    err = L.mla_device_error()
+    assert err in (2, 3)                               # the bad page of request 1 may report first
+    assert torch.all(out[2] == 0) and torch.all(torch.isneginf(lse[2]))
+
+
 def test_lse_optional_and_deterministic(L, impl):
     case = synth.workload_case("tp8_batch", reduced=True).to("cuda")
     o1, l1 = supported(L, impl, case, 0)
