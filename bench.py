@@ -221,11 +221,11 @@ def run_ours(args):
     from mla_latent_kv_fp8_gb300 import _lib, synth
 
     rank, world, local = dist_env()
+    torch.cuda.set_device(local)  # before the process group, so NCCL binds this rank's GPU
+    dev = torch.device("cuda", local)
     if world > 1:
         import torch.distributed as dist
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
+        dist.init_process_group("nccl", device_id=dev)
     L = _lib
     L.lib()
     impl = {"auto": 0, "simt": 1, "tcgen05": 2}[args.kernel]
@@ -254,7 +254,7 @@ def run_ours(args):
 
     def barrier():
         if world > 1:
-            torch.distributed.barrier()
+            torch.distributed.barrier(device_ids=[local])
         torch.cuda.synchronize(dev)
 
     for i in range(args.warmup):
