@@ -178,6 +178,37 @@ def test_out_of_range_page_id_and_seq_len_are_masked_and_reported(L, impl):
     assert torch.all(out[2] == 0) and torch.all(torch.isneginf(lse[2]))
 
 
+def test_many_short_requests(L, impl):
+    """A thousand requests of 32..200 positions in one call (1,000 grid rows of CTAs,
+    12,000 merge rows when split).  (With a single visible position the answer is
+    that position's value, up to ~4.5 in magnitude, where bf16 rounding alone
+    exceeds the 1e-2 absolute bound; those cases are covered at small B.)"""
+    rng = np.random.default_rng(1000)
+    lens = [int(x) for x in rng.integers(32, 201, size=1000)]
+    case = synth.make_decode_case(1000, lens, 12, 1)
+    for n_splits in (0, 3):
+        out, lse = supported(L, impl, case.to("cuda"), n_splits)
+        ro, rl = oracle_full(case)
+        assert_parity(out, lse, ro, rl, what=f"1,000 requests, splits={n_splits}")
+
+
+def test_zero_query_heads_give_the_uniform_average(L, impl):
+    """Heads whose query is all zero score every position 0: the answer is the plain
+    mean of the visible values and lse = ln n (the oracle's closed-form pin)."""
+    lens = [777, 64, 3]
+    case = synth.make_decode_case(1001, lens, 16, 1)
+    q = case.q.clone()
+    q[:, :, 3] = 0
+    q[:, :, 11] = 0
+    case.q = q
+    out, lse = supported(L, impl, case.to("cuda"), 0)
+    ro, rl = oracle_full(case)
+    assert_parity(out, lse, ro, rl, what="zero query heads")
+    got = lse.cpu().numpy()[:, 0, [3, 11]]
+    np.testing.assert_allclose(got, np.log(np.array(lens, dtype=np.float64))[:, None].repeat(2, 1),
+                               atol=1e-4)
+
+
 def test_lse_optional_and_deterministic(L, impl):
     case = synth.workload_case("tp8_batch", reduced=True).to("cuda")
     o1, l1 = supported(L, impl, case, 0)
