@@ -409,6 +409,43 @@ def run_ours(args):
                          "note": "the same step (copy in, decode, copy out) replayed as one CUDA graph, "
                                  "synchronised every step"}}
 
+    # ---- the DCP shard merge (mla_merge_partials over 8 shards' answers) ----
+    dcp_merge = None
+    if args.workload == "dcp_shard" and not args.no_append:
+        S_sh = 8
+        g_m = torch.Generator(device=dev).manual_seed(33)
+        po = (0.25 * torch.randn((S_sh, B, T, H, 512), generator=g_m, device=dev)).to(torch.bfloat16)
+        pl = torch.randn((S_sh, B, T, H), generator=g_m, device=dev) * 3
+        # rotate copies of the shards' answers so that each call reads HBM, not L2
+        n_rot = max(2, -(-3 * l2 // (po.numel() * 2)))
+        pos = [po] + [po.clone() for _ in range(n_rot - 1)]
+        mo = torch.empty((B, T, H, 512), dtype=torch.bfloat16, device=dev)
+        ml = torch.empty((B, T, H), dtype=torch.float32, device=dev)
+        for i in range(5):
+            L.mla_merge_partials(pos[i % n_rot], pl, S_sh, mo, ml, stream)
+        barrier()
+        gm = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gm, stream=stream):
+            for i in range(50):
+                L.mla_merge_partials(pos[i % n_rot], pl, S_sh, mo, ml, stream)
+        with torch.cuda.stream(stream):
+            gm.replay()
+        barrier()
+        ev0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(10):
+                gm.replay()
+        ev1.record(stream)
+        barrier()
+        m_us = ev0.elapsed_time(ev1) * 1e3 / 500
+        m_bytes = po.numel() * 2 + pl.numel() * 4 + mo.numel() * 2 + ml.numel() * 4
+        dcp_merge = {"us_per_call": round(m_us, 3), "bytes_per_call": m_bytes,
+                     "gbps": round(m_bytes / (m_us * 1e-6) / 1e9, 1),
+                     "frac_of_measured_hbm": round(m_bytes / (m_us * 1e-6) / 1e9 / load_peaks()[0], 4),
+                     "note": f"mla_merge_partials of {S_sh} shards' bf16 answers and lse "
+                             f"([{S_sh}, {B}, {T}, {H}, 512]) into one, CUDA-graph replays of 50 calls "
+                             f"over {n_rot} rotating copies of the answers (> 3x L2)"}
+
     # ---- the latent append that precedes each decode step (one call) ----
     append = None
     if not args.no_append:
@@ -472,6 +509,7 @@ def run_ours(args):
             "e2e": e2e,
             "stream_ceiling": ceiling,
             "append": append,
+            "dcp_merge": dcp_merge,
             "gpu_launches": args.steps * (1 + (1 if n_eff > 1 else 0)),
             "clocks": clocks,
         }

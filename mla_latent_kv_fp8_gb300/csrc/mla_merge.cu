@@ -9,8 +9,11 @@
 //     out = sum_s exp(lse_s - lse) * o_s
 // Parts with lse_s = -inf weigh exactly 0; their values are never multiplied.
 //
-// Two kernels:
-//   * few parts (S <= 32): one warp per (row, 64 value dims); lane s holds
+// Three kernels:
+//   * many rows (>= 1,216) and few parts (S <= 32): one warp per whole row,
+//     16 dims per lane, 16-byte loads of up to 8 parts in flight per lane --
+//     the HBM-bound DCP merge and the split combine of large batches;
+//   * few parts (S <= 32), fewer rows: one warp per (row, 64 value dims); lane s holds
 //     lse_s, the normaliser is a shuffle reduction, each lane loads 2 dims of
 //     every part, all parts in one round;
 //   * many parts (S > 32, the in-GPU split combine of one long request): one
@@ -43,6 +46,14 @@ __global__ void __launch_bounds__(256) merge_warp_kernel(MergeParams p) {
 }
 
 template <bool kBf16In>
+__global__ void __launch_bounds__(256) merge_row_kernel(MergeParams p) {
+    wait_for_producer(p.pdl);
+    const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (row >= p.rows) return;
+    merge_row<kBf16In>(p, row, threadIdx.x & 31);
+}
+
+template <bool kBf16In>
 __global__ void __launch_bounds__(256) merge_cta_kernel(MergeParams p) {
     wait_for_producer(p.pdl);
     __shared__ CtaScratch sh;
@@ -66,10 +77,18 @@ cudaError_t launch_with_pdl(K kernel, dim3 grid, dim3 block, cudaStream_t stream
     return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
+constexpr int64_t kRowPathMinRows = 8 * 152;  // one 8-row CTA per SM of a GB300
+
 }  // namespace
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
     if (p.rows == 0) return cudaSuccess;
+    if (p.S <= 32 && p.rows >= kRowPathMinRows) {
+        // enough rows for a full wave of one-warp-per-row CTAs: stream whole rows
+        const dim3 grid((unsigned)((p.rows + 7) / 8));
+        return p.in_bf16 ? launch_with_pdl(merge_row_kernel<true>, grid, dim3(256), stream, p)
+                         : launch_with_pdl(merge_row_kernel<false>, grid, dim3(256), stream, p);
+    }
     if (p.S <= 32) {
         const int64_t warps = p.rows * 8;
         const dim3 grid((unsigned)((warps + 7) / 8));

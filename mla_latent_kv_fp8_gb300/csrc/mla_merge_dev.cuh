@@ -84,6 +84,91 @@ __device__ __forceinline__ void merge_warp(const MergeParams& p, int64_t row, in
     if (chunk == 0 && lane == 0 && p.lse) p.lse[row] = M + logf(sum);
 }
 
+// Many rows (a DCP merge, or the split combine of a large batch): one warp
+// merges one whole row; lane s holds lse_s (S <= 32) and each lane owns 16
+// consecutive value dims, so every part of the row is read with 16-byte loads
+// (2 per part in bf16, 4 in fp32).  Parts are loaded kR at a time, all loads
+// of a round in flight together; a part of weight 0 is neither loaded nor
+// multiplied.
+template <bool kBf16In>
+__device__ __forceinline__ void unpack16(const uint4 (&v)[kBf16In ? 2 : 4], float (&x)[16]) {
+    if constexpr (kBf16In) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                x[8 * k + 2 * j] = __uint_as_float(w[j] << 16);
+                x[8 * k + 2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            x[4 * k] = __uint_as_float(v[k].x);
+            x[4 * k + 1] = __uint_as_float(v[k].y);
+            x[4 * k + 2] = __uint_as_float(v[k].z);
+            x[4 * k + 3] = __uint_as_float(v[k].w);
+        }
+    }
+}
+
+template <bool kBf16In>
+__device__ __forceinline__ void merge_row(const MergeParams& p, int64_t row, int lane) {
+    constexpr int kVecs = kBf16In ? 2 : 4;   // 16-byte loads per part and lane
+    constexpr int kR = kBf16In ? 8 : 4;      // parts per round
+    const float ls = (lane < p.S) ? p.part_lse[(int64_t)lane * p.rows + row] : -INFINITY;
+    const float M = warp_max(ls);
+    uint4* dst = reinterpret_cast<uint4*>(p.out + row * kDv + 16 * lane);
+    if (M == -INFINITY) {
+        dst[0] = dst[1] = make_uint4(0u, 0u, 0u, 0u);
+        if (lane == 0 && p.lse) p.lse[row] = -INFINITY;
+        return;
+    }
+    const float e = (ls == -INFINITY) ? 0.f : exp2f((ls - M) * kLog2e);
+    const float sum = warp_sum(e);
+    const float w = e / sum;  // lanes >= S: 0
+    const size_t elem = kBf16In ? 2 : 4;
+    const char* base = static_cast<const char*>(p.part_out) + (row * kDv + 16 * lane) * elem;
+    const size_t part_stride = static_cast<size_t>(p.rows) * kDv * elem;
+    float acc[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+    for (int s0 = 0; s0 < p.S; s0 += kR) {
+        uint4 v[kR][kVecs];
+        float ws[kR];
+#pragma unroll
+        for (int j = 0; j < kR; ++j) {
+            const int s = s0 + j;
+            ws[j] = __shfl_sync(0xffffffffu, w, s & 31);
+            if (s >= p.S) ws[j] = 0.f;
+            if (ws[j] != 0.f) {  // warp-uniform
+                const uint4* src = reinterpret_cast<const uint4*>(base + s * part_stride);
+#pragma unroll
+                for (int k = 0; k < kVecs; ++k) v[j][k] = __ldg(src + k);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kR; ++j) {
+            if (ws[j] != 0.f) {
+                float x[16];
+                unpack16<kBf16In>(v[j], x);
+#pragma unroll
+                for (int d = 0; d < 16; ++d) acc[d] = fmaf(ws[j], x[d], acc[d]);
+            }
+        }
+    }
+    uint32_t o[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
+        o[j] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    if (lane == 0 && p.lse) p.lse[row] = M + logf(sum);
+}
+
 struct CtaScratch {             // shared memory of merge_cta
     float m[8];                 // per warp: maximum normaliser of its parts
     float l[8];                 // per warp: sum of exp(lse_s - m) over its parts

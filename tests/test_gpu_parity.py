@@ -357,6 +357,30 @@ def test_merge_partials_matches_oracle(L, S, dtype):
     assert_parity(out, lse, ro, rl, what=f"merge S={S}")
 
 
+@pytest.mark.parametrize("S", [1, 3, 8, 19, 32])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_merge_partials_many_rows_matches_oracle(L, S, dtype):
+    """1,280 rows: the one-warp-per-row streaming path (DCP merges, large split
+    combines), with empty parts and an all-empty row."""
+    g = torch.Generator().manual_seed(100 + S)
+    rows = (40, 32)
+    po = (0.25 * torch.randn((S, *rows, 512), generator=g)).to(dtype)
+    pl = (torch.randn((S, *rows), generator=g) * 3).float()
+    drop = torch.rand((S, *rows), generator=g) < 0.3
+    pl[drop] = float("-inf")
+    pl[:, 7, 9] = float("-inf")
+    empty = torch.isinf(pl)
+    po_ref = po.clone()
+    po_ref[empty] = 0
+    po[empty] = float("nan")
+    out = torch.full((*rows, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full(rows, float("nan"), dtype=torch.float32, device="cuda")
+    L.mla_merge_partials(po.cuda(), pl.cuda(), S, out, lse)
+    torch.cuda.synchronize()
+    ro, rl = oracle.merge(po_ref.float().numpy().astype(np.float64), pl.numpy().astype(np.float64))
+    assert_parity(out, lse, ro, rl, what=f"merge S={S}, 1,280 rows")
+
+
 # ----------------------------------------------------------------------------
 # Full-size workloads, launched as the benchmark launches them; sampled rows
 # ----------------------------------------------------------------------------
