@@ -46,7 +46,7 @@ __global__ void __launch_bounds__(256) merge_warp_kernel(MergeParams p) {
 }
 
 template <bool kBf16In>
-__global__ void __launch_bounds__(256) merge_row_kernel(MergeParams p) {
+__global__ void __launch_bounds__(256, kBf16In ? 4 : 2) merge_row_kernel(MergeParams p) {
     wait_for_producer(p.pdl);
     const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (row >= p.rows) return;

@@ -87,9 +87,11 @@ __device__ __forceinline__ void merge_warp(const MergeParams& p, int64_t row, in
 // Many rows (a DCP merge, or the split combine of a large batch): one warp
 // merges one whole row; lane s holds lse_s (S <= 32) and each lane owns 16
 // consecutive value dims, so every part of the row is read with 16-byte loads
-// (2 per part in bf16, 4 in fp32).  Parts are loaded kR at a time, all loads
+// (2 per part in bf16, 4 in fp32).  Parts are loaded four at a time, all loads
 // of a round in flight together; a part of weight 0 is neither loaded nor
-// multiplied.
+// multiplied.  Four parts per round fit 64 registers in bf16 (four CTAs of 256
+// threads per SM) and 128 in fp32 (two per SM); eight bf16 parts per round,
+// at two CTAs per SM, merged 3,072 rows of 8 parts about a quarter slower.
 template <bool kBf16In>
 __device__ __forceinline__ void unpack16(const uint4 (&v)[kBf16In ? 2 : 4], float (&x)[16]) {
     if constexpr (kBf16In) {
@@ -116,7 +118,7 @@ __device__ __forceinline__ void unpack16(const uint4 (&v)[kBf16In ? 2 : 4], floa
 template <bool kBf16In>
 __device__ __forceinline__ void merge_row(const MergeParams& p, int64_t row, int lane) {
     constexpr int kVecs = kBf16In ? 2 : 4;   // 16-byte loads per part and lane
-    constexpr int kR = kBf16In ? 8 : 4;      // parts per round
+    constexpr int kR = 4;                    // parts per round
     const float ls = (lane < p.S) ? p.part_lse[(int64_t)lane * p.rows + row] : -INFINITY;
     const float M = warp_max(ls);
     uint4* dst = reinterpret_cast<uint4*>(p.out + row * kDv + 16 * lane);
