@@ -31,6 +31,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 HBM_NOMINAL_GBS = 8000.0  # the post's and the spec sheet's 8 TB/s
+MLA_LAYERS = 24  # "Kimi K3 on AMD Instinct MI355X" post, the model section: 24 MLA layers
 METRIC = "latent-KV GB/s (KV bytes read / decode-step time); decode steps/s; % of 8 TB/s HBM"
 
 
@@ -278,18 +279,22 @@ def run_ours(args):
     # ---- main timed region: exactly K steps ----
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     n_rep, n_rem = divmod(args.steps, gsteps)
+    # one event after each replay as well, for the spread of the per-step time
+    rep_evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_rep)]
     with ClockSampler(local) as clk:
         barrier()
         ev0.record(stream)
         with torch.cuda.stream(stream):
-            for _ in range(n_rep):
+            for e in rep_evs:
                 graph.replay()
+                e.record(stream)
         for i in range(n_rem):
             step(i)
         ev1.record(stream)
         barrier()
     ms_total = ev0.elapsed_time(ev1)
     assert L.mla_device_error() == 0
+    rep_us = sorted(a.elapsed_time(b_) * 1e3 / gsteps for a, b_ in zip([ev0] + rep_evs[:-1], rep_evs))
 
     # ---- the same steps as individual API calls (host launch cost included) ----
     kdirect = min(args.steps, 2000)
@@ -326,7 +331,9 @@ def run_ours(args):
                 "frac": round(achieved / peak, 4), "traffic": ncu_traffic(family, args.workload),
                 "peak_source": peak_src, "kernel": f"{family} split-KV decode",
                 "kernel_avg_us": round(k_avg_ms * 1e3, 2),
+                "kernel_p10_us": round(kernel_ms[len(kernel_ms) // 10] * 1e3, 2),
                 "kernel_p50_us": round(kernel_ms[len(kernel_ms) // 2] * 1e3, 2),
+                "kernel_p90_us": round(kernel_ms[(9 * len(kernel_ms)) // 10] * 1e3, 2),
                 "frac_of_8TBps": round(achieved / HBM_NOMINAL_GBS, 4),
                 "algorithmic_bytes_per_launch": kv_bytes}
 
@@ -503,6 +510,15 @@ def run_ours(args):
                              "unit": "GB/s", "ms_per_step": round(ms_direct, 5), "steps": kdirect,
                              "note": "one host API call per step, no graph"},
             "decode_steps_per_s": round(steps_per_s, 1),
+            "model_steps_per_s_attention_only": {
+                "value": round(steps_per_s / MLA_LAYERS, 1), "layers": MLA_LAYERS,
+                "note": "decode steps/s over the model's MLA layers: the attention-only bound on "
+                        "whole-model decode steps/s (each step emits one token per request)"},
+            "step_us_spread": ({"p10": round(rep_us[len(rep_us) // 10], 3),
+                                "p50": round(rep_us[len(rep_us) // 2], 3),
+                                "p90": round(rep_us[(9 * len(rep_us)) // 10], 3),
+                                "per": f"mean step of each replay of {gsteps} calls ({len(rep_us)} replays)"}
+                               if rep_us else None),
             "frac_of_8TBps": round(value / HBM_NOMINAL_GBS, 4),
             "roofline": roofline,
             "cpu_baseline": cpu,
