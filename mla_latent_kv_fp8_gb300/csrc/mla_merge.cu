@@ -11,8 +11,9 @@
 //
 // Three kernels:
 //   * many rows (>= 1,216) and few parts (S <= 32): one warp per whole row,
-//     16 dims per lane, 16-byte loads of up to 8 parts in flight per lane --
-//     the HBM-bound DCP merge and the split combine of large batches;
+//     16 dims per lane, 16-byte loads of four parts per round in flight, the
+//     first round issued with the normaliser loads -- the HBM-bound DCP merge
+//     and the split combine of large batches;
 //   * few parts (S <= 32), fewer rows: one warp per (row, 64 value dims); lane s holds
 //     lse_s, the normaliser is a shuffle reduction, each lane loads 2 dims of
 //     every part, all parts in one round;
@@ -46,7 +47,7 @@ __global__ void __launch_bounds__(256) merge_warp_kernel(MergeParams p) {
 }
 
 template <bool kBf16In>
-__global__ void __launch_bounds__(256, kBf16In ? 4 : 2) merge_row_kernel(MergeParams p) {
+__global__ void __launch_bounds__(256, kBf16In ? 3 : 2) merge_row_kernel(MergeParams p) {
     wait_for_producer(p.pdl);
     const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (row >= p.rows) return;
