@@ -47,7 +47,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-ceiling", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-append", action="store_true")
+    ap.add_argument("--no-append", action="store_true",
+                    help="skip the append, DCP merge and DCP verify side measurements")
     return ap.parse_args()
 
 
@@ -453,6 +454,11 @@ def run_ours(args):
                              f"([{S_sh}, {B}, {T}, {H}, 512]) into one, CUDA-graph replays of 50 calls "
                              f"over {n_rot} rotating copies of the answers (> 3x L2)"}
 
+    # ---- DCP multi-token verify: one rank's share of an 8-way split of this workload ----
+    dcp_verify = None
+    if args.workload == "verify" and not args.no_append:
+        dcp_verify = time_dcp_verify(L, base, caches, stream, barrier, l2, dev)
+
     # ---- the latent append that precedes each decode step (one call) ----
     append = None
     if not args.no_append:
@@ -526,12 +532,120 @@ def run_ours(args):
             "stream_ceiling": ceiling,
             "append": append,
             "dcp_merge": dcp_merge,
+            "dcp_verify": dcp_verify,
             "gpu_launches": args.steps * (1 + (1 if n_eff > 1 else 0)),
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def dcp_verify_plan(lens, block_table, n_sh, T):
+    """Contiguous, page-aligned shards of every history for a multi-token verify:
+    shards 0..n_sh-2 hold ceil(L / (64 n_sh)) pages each, the last shard the rest
+    (with the T draft positions at its end).  Returns one (block table, lengths)
+    pair of int32 CPU tensors per shard, each table holding the shard's pages."""
+    import torch
+    B = len(lens)
+    sh_pages = [-(-n // (n_sh * 64)) for n in lens]
+    tails = [n - (n_sh - 1) * 64 * sp for n, sp in zip(lens, sh_pages)]
+    if min(tails) < T:
+        raise ValueError("a history too short for this many shards")
+
+    def table(offsets, widths):
+        t = torch.zeros((B, max(widths)), dtype=torch.int32)
+        for b in range(B):
+            t[b, :widths[b]] = block_table[b, offsets[b]:offsets[b] + widths[b]]
+        return t
+
+    plan = [(table([s * sp for sp in sh_pages], sh_pages),
+             torch.tensor([64 * sp for sp in sh_pages], dtype=torch.int32)) for s in range(n_sh - 1)]
+    plan.append((table([(n_sh - 1) * sp for sp in sh_pages], [-(-n // 64) for n in tails]),
+                 torch.tensor(tails, dtype=torch.int32)))
+    return plan
+
+
+def time_dcp_verify(L, base, caches, stream, barrier, l2, dev, n_sh=8, reps=8):
+    """One rank's step of a multi-token verify split over n_sh contiguous shards of
+    every history (page-aligned; the T draft positions lie in the last shard).  A
+    shard before the last is decoded as T = 1 with T*H rows, the last one with the
+    causal rule, then the n_sh bf16 answers are merged.  All shards of all ranks are
+    timed here on one GPU, each call reading its own pages from HBM; the exchange of
+    answers between GPUs is not part of it."""
+    import torch
+    B, T, H = base.B, base.T, base.H
+    plan = dcp_verify_plan([int(x) for x in base.seq_lens.cpu().tolist()], base.block_table.cpu(), n_sh, T)
+    shard_bt = [t.to(dev) for t, _ in plan[:-1]]
+    sh_lens = plan[0][1].to(dev)
+    tail_bt, tail_lens = plan[-1][0].to(dev), plan[-1][1].to(dev)
+    tails = plan[-1][1].tolist()
+    q1 = base.q.reshape(B, 1, T * H, 576)
+    o1 = torch.empty((B, 1, T * H, 512), dtype=torch.bfloat16, device=dev)
+    l1 = torch.empty((B, 1, T * H), dtype=torch.float32, device=dev)
+    ot = torch.empty((B, T, H, 512), dtype=torch.bfloat16, device=dev)
+    lt = torch.empty((B, T, H), dtype=torch.float32, device=dev)
+    nc = len(caches)
+
+    def shard_call(i):  # shard i % (n_sh - 1), cache copy i // (n_sh - 1): new pages every call
+        L.mla_decode_paged(q1, caches[(i // (n_sh - 1)) % nc], base.kv_scale, shard_bt[i % (n_sh - 1)],
+                           sh_lens, 0, base.sm_scale, o1, l1, stream)
+
+    # the last shard is one region of the cache: enough copies of it to defeat L2
+    tail_bytes = sum(tails) * 576
+    tail_caches = list(caches) + [caches[0].clone()
+                                  for _ in range(max(0, -(-3 * l2 // tail_bytes) - nc))]
+
+    def tail_call(i):
+        L.mla_decode_paged(base.q, tail_caches[i % len(tail_caches)], base.kv_scale, tail_bt, tail_lens,
+                           0, base.sm_scale, ot, lt, stream)
+
+    g_m = torch.Generator(device=dev).manual_seed(44)
+    po = (0.25 * torch.randn((n_sh, B, T, H, 512), generator=g_m, device=dev)).to(torch.bfloat16)
+    pl = torch.randn((n_sh, B, T, H), generator=g_m, device=dev) * 3
+    n_rot = max(2, -(-3 * l2 // (po.numel() * 2)))
+    pos = [po] + [po.clone() for _ in range(n_rot - 1)]
+    mo = torch.empty((B, T, H, 512), dtype=torch.bfloat16, device=dev)
+    ml = torch.empty((B, T, H), dtype=torch.float32, device=dev)
+
+    def merge_call(i):
+        L.mla_merge_partials(pos[i % n_rot], pl, n_sh, mo, ml, stream)
+
+    def per_call_us(fn, n):
+        for i in range(3):
+            fn(i)
+        barrier()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                fn(i)
+        with torch.cuda.stream(stream):
+            g.replay()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(reps):
+                g.replay()
+        e1.record(stream)
+        barrier()
+        return e0.elapsed_time(e1) * 1e3 / (reps * n)
+
+    a = per_call_us(shard_call, (n_sh - 1) * nc * 2)
+    b_ = per_call_us(tail_call, len(tail_caches) * 2)
+    c = per_call_us(merge_call, 50)
+    assert L.mla_device_error() == 0
+    step = max(a, b_) + c
+    kv = base.kv_bytes()
+    return {"shards": n_sh, "shard_call_us": round(a, 2), "last_shard_call_us": round(b_, 2),
+            "merge_us": round(c, 2), "rank_step_us": round(step, 2),
+            "kv_gbps_per_rank": round(kv / n_sh / (step * 1e-6) / 1e9, 1),
+            "job_kv_gbps": round(kv / (step * 1e-6) / 1e9, 1),
+            "note": f"one rank's step: its shard decoded (a shard before the last as T = 1 with "
+                    f"{T * H} rows, the last causal), then mla_merge_partials of the {n_sh} bf16 "
+                    f"answers; each part timed as CUDA-graph replays on this GPU, shards and cache "
+                    f"copies rotated so every call reads HBM; the exchange of answers between GPUs "
+                    f"is not included; job_kv_gbps = all {n_sh} shards' KV bytes / the rank step"}
 
 
 def cpu_baseline(case, budget_s=15.0):

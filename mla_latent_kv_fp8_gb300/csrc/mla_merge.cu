@@ -10,10 +10,10 @@
 // Parts with lse_s = -inf weigh exactly 0; their values are never multiplied.
 //
 // Three kernels:
-//   * many rows (>= 1,216) and few parts (S <= 32): one warp per whole row,
-//     16 dims per lane, 16-byte loads of four parts per round in flight, the
-//     first round issued with the normaliser loads -- the HBM-bound DCP merge
-//     and the split combine of large batches;
+//   * many rows (>= 1,216; >= 256 for bf16 parts) and few parts (S <= 32):
+//     one warp per whole row, 16 dims per lane, 16-byte loads of four parts
+//     per round in flight, the first round issued with the normaliser loads --
+//     the HBM-bound DCP merge and the split combine of large batches;
 //   * few parts (S <= 32), fewer rows: one warp per (row, 64 value dims); lane s holds
 //     lse_s, the normaliser is a shuffle reduction, each lane loads 2 dims of
 //     every part, all parts in one round;
@@ -78,13 +78,21 @@ cudaError_t launch_with_pdl(K kernel, dim3 grid, dim3 block, cudaStream_t stream
     return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
-constexpr int64_t kRowPathMinRows = 8 * 152;  // one 8-row CTA per SM of a GB300
+// Rows from which the one-warp-per-row kernel takes a merge of S <= 32 parts.
+// fp32 parts (the decode's own split combine): one 8-row CTA per SM of a GB300;
+// below that the (row, 64 dims) warps finish sooner inside a decode step (768
+// rows x 14 parts: 179.7 vs 180.8 us per verify step; 96 rows x 19 parts: 3.4
+// vs 10.5 us alone).  bf16 parts (answers of DCP shards) move only 4 bytes per
+// lane and part on the warp path, so the row kernel wins from far fewer rows
+// (768 rows x 8 parts: 4.7 vs 10.3 us).
+constexpr int64_t kRowPathMinRows = 8 * 152;
+constexpr int64_t kRowPathMinRowsBf16 = 256;
 
 }  // namespace
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
     if (p.rows == 0) return cudaSuccess;
-    if (p.S <= 32 && p.rows >= kRowPathMinRows) {
+    if (p.S <= 32 && p.rows >= (p.in_bf16 ? kRowPathMinRowsBf16 : kRowPathMinRows)) {
         // enough rows for a full wave of one-warp-per-row CTAs: stream whole rows
         const dim3 grid((unsigned)((p.rows + 7) / 8));
         return p.in_bf16 ? launch_with_pdl(merge_row_kernel<true>, grid, dim3(256), stream, p)

@@ -1,0 +1,36 @@
+"""Host-side logic of bench.py that needs no GPU: the shard plan of the DCP
+multi-token verify measurement."""
+import numpy as np
+import pytest
+import torch
+
+import bench
+from mla_latent_kv_fp8_gb300 import synth
+
+
+@pytest.mark.parametrize("n_sh", [2, 8])
+def test_dcp_verify_plan_covers_each_history_once(n_sh):
+    lens = synth.verify_lens(4)  # the verify workload's contexts
+    B, T = len(lens), 4
+    max_pages = -(-max(lens) // 64)
+    bt = torch.stack([torch.randperm(10 * max_pages)[:max_pages] for _ in range(B)]).to(torch.int32)
+    plan = bench.dcp_verify_plan(lens, bt, n_sh, T)
+    assert len(plan) == n_sh
+    for b, L in enumerate(lens):
+        pages, pos = [], 0
+        for s, (table, sl) in enumerate(plan):
+            n = int(sl[b])
+            if s < n_sh - 1:
+                assert n % 64 == 0  # shards start on page boundaries
+            np_ = -(-n // 64)
+            pages += table[b, :np_].tolist()
+            pos += n
+        assert pos == L  # the shards tile the history exactly
+        assert pages == bt[b, :-(-L // 64)].tolist()  # in order, each page once
+        assert int(plan[-1][1][b]) >= T  # the draft positions lie in the last shard
+
+
+def test_dcp_verify_plan_rejects_short_histories():
+    bt = torch.arange(4, dtype=torch.int32).reshape(1, 4)
+    with pytest.raises(ValueError):
+        bench.dcp_verify_plan([7 * 64 + 2], bt, 8, 4)

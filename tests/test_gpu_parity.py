@@ -357,13 +357,14 @@ def test_merge_partials_matches_oracle(L, S, dtype):
     assert_parity(out, lse, ro, rl, what=f"merge S={S}")
 
 
+@pytest.mark.parametrize("rows", [(40, 32), (12, 32)])
 @pytest.mark.parametrize("S", [1, 3, 8, 19, 32])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-def test_merge_partials_many_rows_matches_oracle(L, S, dtype):
+def test_merge_partials_many_rows_matches_oracle(L, S, dtype, rows):
     """1,280 rows: the one-warp-per-row streaming path (DCP merges, large split
-    combines), with empty parts and an all-empty row."""
+    combines); 384 rows: that path for bf16 parts, the (row, 64 dims) warps for
+    fp32.  With empty parts and an all-empty row."""
     g = torch.Generator().manual_seed(100 + S)
-    rows = (40, 32)
     po = (0.25 * torch.randn((S, *rows, 512), generator=g)).to(dtype)
     pl = (torch.randn((S, *rows), generator=g) * 3).float()
     drop = torch.rand((S, *rows), generator=g) < 0.3
@@ -378,7 +379,7 @@ def test_merge_partials_many_rows_matches_oracle(L, S, dtype):
     L.mla_merge_partials(po.cuda(), pl.cuda(), S, out, lse)
     torch.cuda.synchronize()
     ro, rl = oracle.merge(po_ref.float().numpy().astype(np.float64), pl.numpy().astype(np.float64))
-    assert_parity(out, lse, ro, rl, what=f"merge S={S}, 1,280 rows")
+    assert_parity(out, lse, ro, rl, what=f"merge S={S}, rows {rows}")
 
 
 # ----------------------------------------------------------------------------
