@@ -216,3 +216,24 @@ def test_append_null_scale_and_empty_batch(L):
     assert _call_append(L, a["lat"], a["bt"], a["sp"], a["kv"]) == 0
     a = _good_append(T=0)
     assert _call_append(L, a["lat"], a["bt"], a["sp"], a["kv"]) == 0
+
+
+def test_auto_splits_invariants_over_a_sweep(L):
+    """Over a sweep of batch shapes: the plan is snapped to equal chunks that all
+    start inside the table, no chunk exceeds 160 pages or falls below 2, and a
+    long enough batch of units of at most 16 rows fills most of a wave of SMs."""
+    for B in (1, 2, 3, 8, 16, 31, 64, 128, 1000):
+        for T, H in ((1, 12), (1, 16), (4, 12), (1, 96), (2, 64), (1, 128)):
+            for max_pages in (1, 2, 3, 5, 16, 64, 100, 161, 512, 2219, 6144, 40000):
+                for sm in (148, 152):
+                    s = L.mla_auto_splits(B, T, H, max_pages, sm)
+                    chunk = L.mla_split_chunk_pages(max_pages, s)
+                    assert s >= 1 and chunk >= 1
+                    assert -(-max_pages // chunk) == s
+                    assert chunk <= 160 or s == 1 and max_pages <= 2
+                    if max_pages > 2:
+                        assert chunk >= 2
+                    if T * H <= 16 and max_pages >= 2 * sm:
+                        # enough pages: the (request, partition) units fill most of
+                        # a wave (equal chunks of whole pages can drop a few)
+                        assert B * s >= 0.8 * sm
