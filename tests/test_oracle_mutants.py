@@ -39,6 +39,12 @@ MUTANTS = {
     "append_row_index": ("kv + ((int64_t)page * ORACLE_PAGE + p % ORACLE_PAGE) * ORACLE_DQK;",
                          "kv + ((int64_t)page * ORACLE_PAGE + (p + 1) % ORACLE_PAGE) * ORACLE_DQK;"),
     "append_scale_multiplies": ("float v = f / kv_scale;", "float v = f * kv_scale;"),
+    "lse_in_log2": ("mx[h] + log(z[h]);", "mx[h] + log2(z[h]);"),
+    "output_not_normalised": ("o[d] /= z[h];", "o[d] = o[d];"),
+    "merge_lse_missing_max": ("double total = m + log(sum);", "double total = log(sum);"),
+    "subnormal_exponent": ("ldexp((double)m / 8.0, 1 - 7)", "ldexp((double)m / 8.0, -7)"),
+    "mantissa_width": ("ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp(1.0 + (double)m / 16.0, e - 7)"),
+    "causal_ignored": ("L - J->T + 1 + t;", "L;"),
 }
 
 
