@@ -32,6 +32,12 @@
  * memory for split partials is owned by the library, kept per (device,
  * stream) and grown with stream-ordered allocation on first need.  Calls on
  * one stream are ordered; calls on different streams use different scratch.
+ * CUDA graphs: a call may be captured once an uncaptured call of at least
+ * the same scratch size has run on that stream; a captured call that would
+ * have to grow the scratch returns MLA_ERR_UNSUPPORTED and records nothing.
+ * Scratch that a captured call used is never freed, so the graph stays valid
+ * after later, larger calls on the stream; a graph replayed on another stream
+ * still uses the scratch of the stream it was captured on.
  *
  * Errors: every entry point validates its arguments on the host before any
  * launch and returns a status; mla_last_error() gives a message for the last

@@ -10,6 +10,7 @@
 #include <mutex>
 #include <string>
 #include <utility>
+#include <vector>
 
 #include "../../include/mla_decode.h"
 #include "../../include/mla_decode_testing.h"
@@ -76,12 +77,18 @@ mla_status_t device_info(DeviceInfo** out) {
 
 // Library-owned split scratch, one buffer per (device, stream), grown in
 // stream order so that a buffer is never released while a kernel still uses it.
+// A buffer that a captured CUDA graph uses is never released at all (the graph
+// may be replayed at any later time): growing it retires it instead.  Growing
+// during a capture is refused, so a graph never owns a stream-ordered
+// allocation of the library.
 struct Scratch {
     void* ptr = nullptr;
     size_t bytes = 0;
+    bool in_graph = false;  // used by a call made during stream capture
 };
 std::mutex g_ws_mu;
 std::map<std::pair<int, void*>, Scratch> g_ws;
+std::vector<void*> g_ws_retired;  // kept for the graphs that may still use them
 
 mla_status_t get_scratch(size_t need, cudaStream_t stream, void** out) {
     *out = nullptr;
@@ -89,14 +96,29 @@ mla_status_t get_scratch(size_t need, cudaStream_t stream, void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(stream, &cap);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+    const bool capturing = cap != cudaStreamCaptureStatusNone;
     std::lock_guard<std::mutex> lk(g_ws_mu);
     Scratch& s = g_ws[{dev, static_cast<void*>(stream)}];
     if (s.bytes < need) {
+        if (capturing)
+            return fail(MLA_ERR_UNSUPPORTED,
+                        "the split scratch of this stream must grow to %zu bytes, which cannot happen "
+                        "during stream capture: make one uncaptured call of this size on the stream "
+                        "first",
+                        need);
         if (s.ptr) {
-            e = cudaFreeAsync(s.ptr, stream);
-            if (e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync(scratch)");
+            if (s.in_graph) {
+                g_ws_retired.push_back(s.ptr);
+            } else {
+                e = cudaFreeAsync(s.ptr, stream);
+                if (e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync(scratch)");
+            }
             s.ptr = nullptr;
             s.bytes = 0;
+            s.in_graph = false;
         }
         size_t grow = need + need / 4;
         e = cudaMallocAsync(&s.ptr, grow, stream);
@@ -108,6 +130,7 @@ mla_status_t get_scratch(size_t need, cudaStream_t stream, void** out) {
         }
         s.bytes = grow;
     }
+    if (capturing) s.in_graph = true;
     *out = s.ptr;
     return MLA_OK;
 }

@@ -261,6 +261,92 @@ def test_graph_capture_and_replay_with_new_inputs(L, impl):
         assert_parity(out, lse, ro, rl, what=f"graph replay, inputs of seed {seed}")
 
 
+def _one_page_partitions(L, case, s, out, lse):
+    """A call with one partition per page: a large split scratch (B x T x H
+    rows x 2,052 bytes per partition)."""
+    pages = case.block_table.shape[1]
+    L.mla_decode_paged(case.q, case.kv_cache, case.kv_scale, case.block_table, case.seq_lens, pages,
+                       case.sm_scale, out, lse, s)
+
+
+@pytest.mark.filterwarnings("ignore:The CUDA Graph is empty")  # the refused capture records nothing
+def test_capture_that_would_grow_the_scratch_is_refused(L):
+    """A captured call may not allocate: if the stream's scratch is too small the
+    call is refused with MLA_ERR_UNSUPPORTED and records nothing; after an
+    uncaptured call of that size the same capture works and replays correctly.
+    128 partitions x 4 x 128 rows need ~135 MB, more than any earlier call of
+    the suite made any stream hold."""
+    case = synth.make_decode_case(95, [8192, 8000, 5000, 8192], 128, 1).to("cuda")
+    out = torch.full((4, 1, 128, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((4, 1, 128), float("nan"), device="cuda")
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with pytest.raises(L.MlaError) as ei:
+        with torch.cuda.graph(g, stream=s):
+            _one_page_partitions(L, case, s, out, lse)
+    assert ei.value.status == 2 and "capture" in str(ei.value)
+    with torch.cuda.stream(s):
+        _one_page_partitions(L, case, s, out, lse)  # uncaptured: the scratch grows
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        _one_page_partitions(L, case, s, out, lse)
+    out.fill_(float("nan"))
+    lse.fill_(float("nan"))
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        g.replay()
+    torch.cuda.synchronize()
+    assert L.mla_device_error() == 0
+    reqs, heads = [0, 2], [0, 77, 127]
+    ro, rl = oracle_rows(case, reqs, heads)
+    assert_parity(out[reqs][:, :, heads], lse[reqs][:, :, heads], ro, rl,
+                  what="captured after the scratch grew, sampled rows")
+    assert not torch.isnan(out).any() and not torch.isnan(lse).any()
+
+
+def test_graph_survives_a_later_larger_call(L):
+    """The scratch a captured call used is retired, not freed, when a later
+    uncaptured call on the stream needs more: replaying the graph afterwards
+    still answers correctly."""
+    lens = [1200, 3000]
+    live = synth.make_decode_case(96, lens, 12, 1, extra_pages=2).to("cuda")
+    out = torch.empty((2, 1, 12, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((2, 1, 12), device="cuda")
+    s = torch.cuda.Stream()
+
+    def call():
+        L.mla_decode_paged(live.q, live.kv_cache, live.kv_scale, live.block_table, live.seq_lens, 0,
+                           live.sm_scale, out, lse, s)
+
+    with torch.cuda.stream(s):
+        call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call()
+    # 256 partitions x 4 x 128 rows (~270 MB): the stream's scratch must grow
+    big = synth.make_decode_case(98, [16384] * 4, 128, 1).to("cuda")
+    with torch.cuda.stream(s):
+        _one_page_partitions(L, big, s, torch.empty((4, 1, 128, 512), dtype=torch.bfloat16, device="cuda"),
+                             None)
+    torch.cuda.synchronize()
+    assert L.mla_device_error() == 0
+    src = synth.make_decode_case(97, lens, 12, 1, extra_pages=2)
+    for dst_t, src_t in ((live.q, src.q), (live.kv_cache, src.kv_cache), (live.kv_scale, src.kv_scale),
+                         (live.block_table, src.block_table), (live.seq_lens, src.seq_lens)):
+        dst_t.copy_(src_t)
+    out.fill_(float("nan"))
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        g.replay()
+    torch.cuda.synchronize()
+    assert L.mla_device_error() == 0
+    ro, rl = oracle_full(src)
+    assert_parity(out, lse, ro, rl, what="graph replayed after the stream's scratch grew")
+
+
 def test_two_streams_at_once(L, impl):
     """Calls on two streams run concurrently with their own split scratch."""
     cases = [synth.make_decode_case(81 + k, [3000, 900], 12, 1).to("cuda") for k in range(2)]
