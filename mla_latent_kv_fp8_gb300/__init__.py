@@ -1,8 +1,8 @@
 """GB300-native (sm_103a) MLA decode over a paged FP8 latent-KV cache.
 
 The product is the C ABI library ``libmla_decode.so`` (include/mla_decode.h):
-split-KV decode kernels on tcgen05 tensor cores and CUDA cores, and a
-log-sum-exp merge kernel.  This package holds its sources (``csrc/``), the
+split-KV decode kernels on tcgen05 tensor cores and CUDA cores, the
+log-sum-exp merge kernels and the FP8 latent-append kernel.  This package holds its sources (``csrc/``), the
 in-tree build, the ctypes binding and the seeded synthetic input generators.
 """
 from __future__ import annotations
@@ -34,6 +34,8 @@ def decode(case, n_splits: int = 0, stream=None, out=None, lse=None):
 
 
 def merge_partials(partial_out, partial_lse, stream=None, out=None, lse=None):
+    """Run mla_merge_partials over the leading (shard) dim of ``partial_out``
+    (bf16 or fp32 [S, ..., 512]) and ``partial_lse`` (fp32 [S, ...])."""
     b = _binding()
     S = partial_out.shape[0]
     if out is None:
