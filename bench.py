@@ -44,6 +44,9 @@ def parse():
     ap.add_argument("--workload", default="tp8_batch")
     ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tcgen05"])
     ap.add_argument("--n-splits", type=int, default=0)
+    ap.add_argument("--planner", default="lengths", choices=["lengths", "auto"],
+                    help="split count when --n-splits is 0: mla_plan_splits on the host-known "
+                         "lengths, or mla_auto_splits from max_pages alone")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-ceiling", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -237,6 +240,14 @@ def run_ours(args):
     kv_bytes = base.kv_bytes()
     B, T, H = base.B, base.T, base.H
     n_splits = args.n_splits if args.n_splits > 0 else (4 if args.workload == "tiny" else 0)
+    planner = "explicit" if n_splits > 0 else "mla_auto_splits (from max_pages)"
+    if n_splits == 0 and args.planner == "lengths":
+        # a serving engine knows its batch's lengths on the host: plan once per batch
+        t_plan = time.perf_counter()
+        n_splits = L.mla_plan_splits(B, T, H, base.lens, base.block_table.shape[1], 0)
+        t_plan = time.perf_counter() - t_plan
+        planner = (f"mla_plan_splits from the host lengths, once per batch outside the timed steps "
+                   f"({t_plan * 1e6:.0f} us on the host)")
     # rotate cache copies so that each step reads HBM, not L2
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     n_copies = max(2, -(-3 * l2 // max(base.kv_cache.numel(), 1)))
@@ -506,7 +517,7 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "e4m3fn KV x bf16 q, f32 accumulate", "data": "synthetic",
             "config": {"workload": f"{args.workload}: {workload_description(args.workload)}",
-                       "page": 64, "kv_bytes_per_step": kv_bytes, "n_splits": n_eff,
+                       "page": 64, "kv_bytes_per_step": kv_bytes, "n_splits": n_eff, "planner": planner,
                        "chunk_pages": chunk, "l2": f"{n_copies} rotating cache copies "
                        f"({n_copies * base.kv_cache.numel() / 1e6:.0f} MB > L2 {l2 / 1e6:.0f} MB)",
                        "kernel_family": family,
@@ -587,9 +598,14 @@ def time_dcp_verify(L, base, caches, stream, barrier, l2, dev, n_sh=8, reps=8):
     lt = torch.empty((B, T, H), dtype=torch.float32, device=dev)
     nc = len(caches)
 
+    # each rank plans its call from the lengths it holds (all shards before the last
+    # have the same lengths)
+    ns_shard = L.mla_plan_splits(B, 1, T * H, plan[0][1].tolist(), shard_bt[0].shape[1], 0)
+    ns_tail = L.mla_plan_splits(B, T, H, tails, tail_bt.shape[1], 0)
+
     def shard_call(i):  # shard i % (n_sh - 1), cache copy i // (n_sh - 1): new pages every call
         L.mla_decode_paged(q1, caches[(i // (n_sh - 1)) % nc], base.kv_scale, shard_bt[i % (n_sh - 1)],
-                           sh_lens, 0, base.sm_scale, o1, l1, stream)
+                           sh_lens, ns_shard, base.sm_scale, o1, l1, stream)
 
     # the last shard is one region of the cache: enough copies of it to defeat L2
     tail_bytes = sum(tails) * 576
@@ -598,7 +614,7 @@ def time_dcp_verify(L, base, caches, stream, barrier, l2, dev, n_sh=8, reps=8):
 
     def tail_call(i):
         L.mla_decode_paged(base.q, tail_caches[i % len(tail_caches)], base.kv_scale, tail_bt, tail_lens,
-                           0, base.sm_scale, ot, lt, stream)
+                           ns_tail, base.sm_scale, ot, lt, stream)
 
     g_m = torch.Generator(device=dev).manual_seed(44)
     po = (0.25 * torch.randn((n_sh, B, T, H, 512), generator=g_m, device=dev)).to(torch.bfloat16)
@@ -637,7 +653,9 @@ def time_dcp_verify(L, base, caches, stream, barrier, l2, dev, n_sh=8, reps=8):
     assert L.mla_device_error() == 0
     step = max(a, b_) + c
     kv = base.kv_bytes()
-    return {"shards": n_sh, "shard_call_us": round(a, 2), "last_shard_call_us": round(b_, 2),
+    return {"shards": n_sh, "n_splits": {"shard": ns_shard, "last_shard": ns_tail,
+                                         "planner": "mla_plan_splits on each rank's host lengths"},
+            "shard_call_us": round(a, 2), "last_shard_call_us": round(b_, 2),
             "merge_us": round(c, 2), "rank_step_us": round(step, 2),
             "kv_gbps_per_rank": round(kv / n_sh / (step * 1e-6) / 1e9, 1),
             "job_kv_gbps": round(kv / (step * 1e-6) / 1e9, 1),

@@ -219,6 +219,24 @@ mla_status_t mla_append_latent(const mla_tensor_t *latent, const float *kv_scale
  * Pure host function; sm_count <= 0 means "query the current device". */
 int32_t mla_auto_splits(int32_t B, int32_t T, int32_t H, int32_t max_pages, int32_t sm_count);
 
+/* The split count for a batch whose lengths the caller knows on the host (a
+ * serving engine schedules them): pass the result as n_splits.  For units of
+ * more than 16 rows (the 32-row tensor-core kernel, where a partition costs
+ * its pages at a fixed per-page time plus a fixed set-up and epilogue) it
+ * replays the launch of the (request, partition, row-CTA) grid on the host:
+ * CTAs in launch order, each on the SM that frees first, one per SM, each
+ * costing its pages plus 8, and returns the count with the shortest
+ * finish (ties: fewer partitions), trying counts up to 8 waves of full-length
+ * CTAs.  For units of up to 16 rows (HBM-bound, one wave), or when
+ * host_seq_lens is NULL, it returns mla_auto_splits(B, T, H, max_pages,
+ * sm_count).
+ *   host_seq_lens  host pointer to the B lengths the decode will read from
+ *                  seq_lens (values outside [0, 64 * max_pages] are clamped).
+ *   max_pages      the block table's width, as passed to the decode.
+ * Pure host function; sm_count <= 0 means "query the current device". */
+int32_t mla_plan_splits(int32_t B, int32_t T, int32_t H, const int32_t *host_seq_lens,
+                        int32_t max_pages, int32_t sm_count);
+
 /* Pages per partition for a given split count: ceil(max_pages / n_splits),
  * so that the partitions of a full-length request differ by at most one
  * page, except the last, which takes the remainder. */

@@ -29,7 +29,7 @@ EXPORTS = ("mla_decode_paged", "mla_merge_partials", "mla_auto_splits", "mla_spl
            "mla_decode_workspace_bytes", "mla_set_impl", "mla_device_error", "mla_status_string",
            "mla_last_error", "mla_profile_next_decode", "mla_last_decode_impl",
            "mla_decode_paged_noalloc", "mla_test_stall_copies", "mla_bench_stream_pages",
-           "mla_append_latent")
+           "mla_append_latent", "mla_plan_splits")
 
 
 class MlaError(RuntimeError):
@@ -61,6 +61,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mla_merge_partials.restype = ctypes.c_int
     lib.mla_auto_splits.argtypes = [ctypes.c_int32] * 5
     lib.mla_auto_splits.restype = ctypes.c_int32
+    lib.mla_plan_splits.argtypes = [ctypes.c_int32] * 3 + [ctypes.POINTER(ctypes.c_int32)] + [ctypes.c_int32] * 2
+    lib.mla_plan_splits.restype = ctypes.c_int32
     lib.mla_split_chunk_pages.argtypes = [ctypes.c_int32, ctypes.c_int32]
     lib.mla_split_chunk_pages.restype = ctypes.c_int32
     lib.mla_decode_workspace_bytes.argtypes = [ctypes.c_int32] * 4
@@ -164,6 +166,13 @@ def mla_merge_partials(partial_out, partial_lse, n_shards, out, lse=None, stream
 
 def mla_auto_splits(B, T, H, max_pages, sm_count=0):
     return lib().mla_auto_splits(B, T, H, max_pages, sm_count)
+
+
+def mla_plan_splits(B, T, H, host_seq_lens, max_pages, sm_count=0):
+    """host_seq_lens: B lengths on the host (a sequence of ints, or a CPU int32
+    tensor / array)."""
+    arr = (ctypes.c_int32 * B)(*[int(x) for x in host_seq_lens])
+    return lib().mla_plan_splits(B, T, H, arr, max_pages, sm_count)
 
 
 def mla_split_chunk_pages(max_pages, n_splits):

@@ -2,10 +2,12 @@
 // argument validation, split planning, library-owned scratch, kernel dispatch
 // and error reporting.  Everything here runs on the host; every step of the
 // attention itself runs in the CUDA kernels.
+#include <algorithm>
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <functional>
 #include <map>
 #include <mutex>
 #include <string>
@@ -247,6 +249,65 @@ int32_t mla_auto_splits(int32_t B, int32_t T, int32_t H, int32_t max_pages, int3
     // Snap to the count that equal chunks actually produce.
     const int64_t chunk = mla_split_chunk_pages(max_pages, (int32_t)s);
     return (int32_t)ceil_div(max_pages, chunk);
+}
+
+// Per-CTA fixed cost of a partition in the length-aware plan, in pages of
+// loop time: set-up (~3 us) and epilogue (~2.4 us) of a 32-row CTA against
+// ~0.7 us per page.
+constexpr int64_t kPlanFixedPages = 8;
+
+int32_t mla_plan_splits(int32_t B, int32_t T, int32_t H, const int32_t* host_seq_lens, int32_t max_pages,
+                        int32_t sm_count) {
+    const int32_t fallback = mla_auto_splits(B, T, H, max_pages, sm_count);
+    if (!host_seq_lens || B <= 0 || max_pages <= 2) return fallback;
+    const int64_t rows = (int64_t)(T > 0 ? T : 1) * (H > 0 ? H : 1);
+    if (rows <= 16) return fallback;  // HBM-bound kernel: one wave, lengths do not change it
+    const int64_t G = ceil_div(rows, 32);
+    if (sm_count <= 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            sm_count = 148;
+        }
+    }
+    std::vector<int64_t> pages(B);
+    for (int32_t b = 0; b < B; ++b) {
+        int64_t L = host_seq_lens[b];
+        L = L < 0 ? 0 : (L > (int64_t)max_pages * kPage ? (int64_t)max_pages * kPage : L);
+        pages[b] = ceil_div(L, kPage);
+    }
+    // Candidate counts: up to 8 waves of CTAs at full length (more never pays).
+    const int64_t most = ceil_div(max_pages, 2);
+    int64_t hi = (8 * (int64_t)sm_count) / (B * G);
+    hi = hi < 1 ? 1 : (hi > most ? most : hi);
+    if (hi > 1024) hi = 1024;
+    std::vector<int64_t> load((size_t)sm_count);
+    int64_t best_cost = -1, best = 1, last_chunk = -1;
+    for (int64_t c = 1; c <= hi; ++c) {
+        const int64_t chunk = mla_split_chunk_pages(max_pages, (int32_t)c);
+        if (chunk == last_chunk) continue;  // the same snapped plan as a smaller count
+        last_chunk = chunk;
+        const int64_t n = ceil_div(max_pages, chunk);
+        // CTAs start in launch order (partition and row-CTA fastest, then the
+        // request), each on the SM that frees first, one CTA per SM.
+        std::fill(load.begin(), load.end(), 0);  // all zero: already a heap
+        int64_t cost = 0;                         // the latest finish so far
+        for (int32_t b = 0; b < B && (best_cost < 0 || cost < best_cost); ++b) {
+            for (int64_t sp = 0; sp < n; ++sp) {
+                const int64_t w = std::min(chunk, pages[b] - sp * chunk);
+                if (w <= 0) break;  // partitions past the request's end exit at once
+                for (int64_t r = 0; r < G; ++r) {
+                    std::pop_heap(load.begin(), load.end(), std::greater<int64_t>());
+                    load.back() += w + kPlanFixedPages;
+                    cost = std::max(cost, load.back());
+                    std::push_heap(load.begin(), load.end(), std::greater<int64_t>());
+                }
+            }
+        }
+        if (best_cost < 0 || cost < best_cost) best_cost = cost, best = n;  // a pruned plan never wins
+    }
+    return (int32_t)best;
 }
 
 int32_t mla_split_chunk_pages(int32_t max_pages, int32_t n_splits) {

@@ -5,8 +5,11 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 import torch
+
+from mla_latent_kv_fp8_gb300 import synth
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -237,3 +240,59 @@ def test_auto_splits_invariants_over_a_sweep(L):
                         # enough pages: the (request, partition) units fill most of
                         # a wave (equal chunks of whole pages can drop a few)
                         assert B * s >= 0.8 * sm
+
+
+@pytest.mark.parametrize("B,T,H,max_pages", [
+    (32, 1, 96, 278),    # dcp_shard
+    (16, 4, 12, 1568),   # verify-like, 48 rows
+    (16, 1, 48, 195),    # a DCP-verify shard before the last
+    (3, 2, 64, 700),     # 128 rows, 4 CTAs per unit
+])
+def test_plan_splits_equals_auto_when_every_request_is_full(L, B, T, H, max_pages):
+    """With every request max_pages long the length-aware plan and the automatic
+    one agree (both minimise waves x partition length for uniform work)."""
+    full = [64 * max_pages] * B
+    assert L.mla_plan_splits(B, T, H, full, max_pages, 152) == L.mla_auto_splits(B, T, H, max_pages, 152)
+
+
+def test_plan_splits_falls_back_to_auto(L):
+    lens = [1000, 20000, 5, 0, 70000, 3000, 64, 9000]
+    mp = -(-max(lens) // 64)
+    for T, H in ((1, 12), (1, 16), (2, 8)):  # units of at most 16 rows: one HBM-bound wave
+        assert L.mla_plan_splits(8, T, H, lens, mp, 152) == L.mla_auto_splits(8, T, H, mp, 152)
+    assert L.lib().mla_plan_splits(8, 4, 12, None, mp, 152) == L.mla_auto_splits(8, 4, 12, mp, 152)
+    assert L.mla_plan_splits(0, 4, 12, [], mp, 152) == L.mla_auto_splits(0, 4, 12, mp, 152)
+
+
+def test_plan_splits_ragged_batches(L):
+    """Short, uneven histories: the plan takes more partitions than the
+    max_pages-based count, because short requests leave SMs free.  On the
+    verify workload's 8-way DCP shards (16 requests x 48 rows, 16..195 pages)
+    it picks 7 partitions, and 16 on the whole verify workload: the fastest
+    counts of a sweep on GB300 (shards: 38.4 us at 7 against 40.6 at 6, 44.1
+    at 8 and 50.2 at the automatic 4; whole workload: 168 us at 16 against 180
+    at the automatic 14 and 212 at 18)."""
+    import bench
+    lens = synth.verify_lens(4)
+    Lb = L
+    plan = bench.dcp_verify_plan(lens, torch.zeros((16, 2048), dtype=torch.int32), 8, 4)
+    for (table, sl), (T, H) in ((plan[0], (1, 48)), (plan[-1], (4, 12))):
+        assert Lb.mla_plan_splits(16, T, H, sl.tolist(), table.shape[1], 152) == 7
+    mp = -(-max(lens) // 64)
+    assert Lb.mla_plan_splits(16, 4, 12, lens, mp, 152) == 16
+    assert Lb.mla_auto_splits(16, 4, 12, mp, 152) == 14
+
+
+def test_plan_splits_is_a_valid_plan_over_a_sweep(L):
+    rng = np.random.default_rng(5)
+    for _ in range(200):
+        B = int(rng.integers(1, 40))
+        T = int(rng.choice([1, 2, 4, 8]))
+        H = int(rng.integers(1, 128 // T + 1))
+        lens = [int(x) for x in rng.integers(-5, 200_000, size=B)]
+        mp = max(1, -(-max(max(lens), 0) // 64) + int(rng.integers(0, 3)))
+        n = L.mla_plan_splits(B, T, H, lens, mp, int(rng.choice([148, 152])))
+        chunk = L.mla_split_chunk_pages(mp, n)
+        assert 1 <= n and -(-mp // chunk) == n
+        if mp > 2:
+            assert n <= -(-mp // 2)
