@@ -108,7 +108,9 @@ typedef enum {
  *               new positions; 0 (empty history) gives out = 0, lse = -inf;
  *               must be <= 64 * max_pages, and >= T unless 0.
  *   n_splits    > 0: use exactly this many history partitions per request;
- *               0: choose automatically to fill every SM (mla_auto_splits).
+ *               0: choose automatically to fill every SM (mla_auto_splits);
+ *               a caller that knows the lengths on the host can pass
+ *               mla_plan_splits(...) instead.
  *   sm_scale    softmax scale applied to q . x (e.g. 1/sqrt(192)).
  *   out         bf16 [B, T, H, 512], device, contiguous, caller-allocated;
  *               out = sum_p softmax_p * x_p[0:512], rounded to nearest even.
