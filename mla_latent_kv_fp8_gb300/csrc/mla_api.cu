@@ -277,25 +277,42 @@ int32_t mla_plan_splits(int32_t B, int32_t T, int32_t H, const int32_t* host_seq
         L = L < 0 ? 0 : (L > (int64_t)max_pages * kPage ? (int64_t)max_pages * kPage : L);
         pages[b] = ceil_div(L, kPage);
     }
-    // Candidate counts: up to 8 waves of CTAs at full length (more never pays).
+    // Candidate counts: up to 8 waves of CTAs at full length (more never pays),
+    // one per distinct chunk size.  Each has a lower bound on its finish (its
+    // longest CTA, and its total work spread over every SM); candidates are
+    // replayed in the order of that bound until the bound passes the best
+    // finish found, which gives the same answer as replaying them all.
     const int64_t most = ceil_div(max_pages, 2);
     int64_t hi = (8 * (int64_t)sm_count) / (B * G);
     hi = hi < 1 ? 1 : (hi > most ? most : hi);
     if (hi > 1024) hi = 1024;
-    std::vector<int64_t> load((size_t)sm_count);
-    int64_t best_cost = -1, best = 1, last_chunk = -1;
-    for (int64_t c = 1; c <= hi; ++c) {
+    const int64_t longest = *std::max_element(pages.begin(), pages.end());
+    struct Cand {
+        int64_t bound, n, chunk;
+    };
+    std::vector<Cand> cands;
+    for (int64_t c = 1, last_chunk = -1; c <= hi; ++c) {
         const int64_t chunk = mla_split_chunk_pages(max_pages, (int32_t)c);
         if (chunk == last_chunk) continue;  // the same snapped plan as a smaller count
         last_chunk = chunk;
-        const int64_t n = ceil_div(max_pages, chunk);
+        int64_t work = 0;
+        for (int64_t p : pages) work += p + ceil_div(p, chunk) * kPlanFixedPages;
+        const int64_t bound = std::max(std::min(chunk, longest) + kPlanFixedPages, ceil_div(G * work, sm_count));
+        cands.push_back({bound, ceil_div(max_pages, chunk), chunk});
+    }
+    std::sort(cands.begin(), cands.end(),
+              [](const Cand& a, const Cand& b) { return a.bound != b.bound ? a.bound < b.bound : a.n < b.n; });
+    std::vector<int64_t> load((size_t)sm_count);
+    int64_t best_cost = -1, best = 1;
+    for (const Cand& cd : cands) {
+        if (best_cost >= 0 && (cd.bound > best_cost || (cd.bound == best_cost && cd.n > best))) break;
         // CTAs start in launch order (partition and row-CTA fastest, then the
         // request), each on the SM that frees first, one CTA per SM.
         std::fill(load.begin(), load.end(), 0);  // all zero: already a heap
         int64_t cost = 0;                         // the latest finish so far
-        for (int32_t b = 0; b < B && (best_cost < 0 || cost < best_cost); ++b) {
-            for (int64_t sp = 0; sp < n; ++sp) {
-                const int64_t w = std::min(chunk, pages[b] - sp * chunk);
+        for (int32_t b = 0; b < B; ++b) {
+            for (int64_t sp = 0; sp < cd.n; ++sp) {
+                const int64_t w = std::min(cd.chunk, pages[b] - sp * cd.chunk);
                 if (w <= 0) break;  // partitions past the request's end exit at once
                 for (int64_t r = 0; r < G; ++r) {
                     std::pop_heap(load.begin(), load.end(), std::greater<int64_t>());
@@ -305,7 +322,7 @@ int32_t mla_plan_splits(int32_t B, int32_t T, int32_t H, const int32_t* host_seq
                 }
             }
         }
-        if (best_cost < 0 || cost < best_cost) best_cost = cost, best = n;  // a pruned plan never wins
+        if (best_cost < 0 || cost < best_cost || (cost == best_cost && cd.n < best)) best_cost = cost, best = cd.n;
     }
     return (int32_t)best;
 }

@@ -296,3 +296,50 @@ def test_plan_splits_is_a_valid_plan_over_a_sweep(L):
         assert 1 <= n and -(-mp // chunk) == n
         if mp > 2:
             assert n <= -(-mp // 2)
+
+
+def _plan_by_replay(B, T, H, lens, max_pages, sm):
+    """The length-aware plan written out plainly: every candidate count (one per
+    distinct chunk size, up to 8 full-length waves) replayed in launch order on
+    a min-heap of SM finish times; the earliest finish wins, ties to fewer
+    partitions."""
+    import heapq
+    G = -(-(T * H) // 32)
+    pages = [-(-min(max(x, 0), 64 * max_pages) // 64) for x in lens]
+    most = -(-max_pages // 2)
+    hi = max(1, min(most, (8 * sm) // (B * G), 1024))
+    best = None
+    seen = set()
+    for c in range(1, hi + 1):
+        chunk = max(1, -(-max_pages // c))
+        if chunk in seen:
+            continue
+        seen.add(chunk)
+        n = -(-max_pages // chunk)
+        heap = [0] * sm
+        finish = 0
+        for p in pages:
+            for s in range(n):
+                w = min(chunk, p - s * chunk)
+                if w <= 0:
+                    break
+                for _ in range(G):
+                    t = heapq.heappop(heap) + w + 8
+                    finish = max(finish, t)
+                    heapq.heappush(heap, t)
+        if best is None or (finish, n) < best:
+            best = (finish, n)
+    return best[1]
+
+
+def test_plan_splits_matches_a_plain_replay(L):
+    """The library's pruned search returns what replaying every candidate returns."""
+    rng = np.random.default_rng(11)
+    for _ in range(60):
+        B = int(rng.integers(1, 40))
+        T = int(rng.choice([1, 2, 4]))
+        H = int(rng.integers(17 // T + 1, 128 // T + 1))  # more than 16 rows
+        lens = [int(x) for x in rng.integers(0, int(rng.choice([3000, 40000, 150000])), size=B)]
+        mp = max(3, -(-max(lens) // 64))
+        sm = int(rng.choice([148, 152]))
+        assert L.mla_plan_splits(B, T, H, lens, mp, sm) == _plan_by_replay(B, T, H, lens, mp, sm), (B, T, H, mp)
