@@ -507,7 +507,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(base, budget_s=15.0)
+        cpu = cpu_baseline(base, budget_s=15.0, out=out, lse=lse)
 
     if rank == 0:
         clocks = clk.summary()
@@ -666,9 +666,11 @@ def time_dcp_verify(L, base, caches, stream, barrier, l2, dev, n_sh=8, reps=8):
                     f"is not included; job_kv_gbps = all {n_sh} shards' KV bytes / the rank step"}
 
 
-def cpu_baseline(case, budget_s=15.0):
+def cpu_baseline(case, budget_s=15.0, out=None, lse=None):
     """The FP64 oracle as it stands, on this host's cores, over a bounded sample of
-    the same workload (whole requests, all heads), reported in the same unit."""
+    the same workload (whole requests, all heads), reported in the same unit.
+    Given the device answer of the timed steps (out, lse), the sampled requests'
+    rows are also compared with the oracle's (the parity tolerances)."""
     import numpy as np
     import oracle
     c = case.to("cpu")
@@ -678,13 +680,36 @@ def cpu_baseline(case, budget_s=15.0):
     t1 = time.perf_counter() - t0
     n_req = int(max(1, min(c.B, budget_s / max(t1, 1e-3) * max(os.cpu_count() or 1, 1) / 2)))
     t0 = time.perf_counter()
-    _, _, threads = oracle.decode(c.q[:n_req], c.kv_cache, c.kv_scale, c.block_table[:n_req],
-                                  c.seq_lens[:n_req], c.sm_scale, return_threads=True)
+    ro, rl, threads = oracle.decode(c.q[:n_req], c.kv_cache, c.kv_scale, c.block_table[:n_req],
+                                    c.seq_lens[:n_req], c.sm_scale, return_threads=True)
     dt = time.perf_counter() - t0
     kvb = 576 * int(np.sum(c.lens[:n_req]))
-    return {"value": round(kvb / dt / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"{n_req} of {c.B} requests (all heads, full context), {dt:.2f} s",
-            "seconds": round(dt, 3)}
+    res = {"value": round(kvb / dt / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+           "sample": f"{n_req} of {c.B} requests (all heads, full context), {dt:.2f} s",
+           "seconds": round(dt, 3)}
+    if out is not None and lse is not None:
+        res["parity"] = parity_of(out[:n_req].float().cpu().numpy(), lse[:n_req].cpu().numpy(), ro, rl)
+    return res
+
+
+def parity_of(o, l, ro, rl):
+    """Errors of a device answer against the oracle's on the same rows, and whether
+    they meet the tolerances (max|dout| <= 1e-2, max|dout| / max|out| <= 1.6e-2,
+    max|dlse| <= 1e-4; empty rows must be out = 0, lse = -inf)."""
+    import numpy as np
+    empty = np.isneginf(rl)
+    full = ~empty
+    res = {"rows": int(rl.size), "empty_rows": int(empty.sum())}
+    ok = bool(np.all(o[empty] == 0) and np.all(np.isneginf(l[empty])))
+    if full.any():
+        d = np.abs(o[full] - ro[full])
+        res["max_abs_out"] = float(d.max())
+        res["rel_out"] = float(d.max() / max(float(np.abs(ro[full]).max()), 1e-30))
+        res["max_abs_lse"] = float(np.abs(l[full] - rl[full]).max())
+        ok = ok and bool(np.isfinite(o[full]).all() and np.isfinite(l[full]).all())
+        ok = ok and res["max_abs_out"] <= 1e-2 and res["rel_out"] <= 1.6e-2 and res["max_abs_lse"] <= 1e-4
+    res["pass"] = ok
+    return res
 
 
 def run_reference(args):
