@@ -34,3 +34,23 @@ def test_dcp_verify_plan_rejects_short_histories():
     bt = torch.arange(4, dtype=torch.int32).reshape(1, 4)
     with pytest.raises(ValueError):
         bench.dcp_verify_plan([7 * 64 + 2], bt, 8, 4)
+
+
+def test_parity_of_applies_the_tolerances():
+    ro = np.zeros((2, 1, 3, 512))
+    ro[0] = 0.5
+    rl = np.array([[[1.0, 2.0, 3.0]], [[-np.inf] * 3]])
+    o, l = ro.copy(), rl.copy()
+    assert bench.parity_of(o, l, ro, rl)["pass"]
+    o2 = o.copy()
+    o2[0, 0, 1, 7] += 0.011  # above the 1e-2 absolute bound
+    assert not bench.parity_of(o2, l, ro, rl)["pass"]
+    l2 = l.copy()
+    l2[0, 0, 2] += 2e-4  # above the 1e-4 LSE bound
+    assert not bench.parity_of(o, l2, ro, rl)["pass"]
+    o3 = o.copy()
+    o3[1, 0, 0, 0] = 1e-3  # an empty row must be exactly 0
+    assert not bench.parity_of(o3, l, ro, rl)["pass"]
+    o4 = o.copy()
+    o4[0, 0, 0, 0] = np.nan
+    assert not bench.parity_of(o4, l, ro, rl)["pass"]
