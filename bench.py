@@ -92,6 +92,34 @@ def load_peaks():
     return 6800.0, "fallback (6.8 TB/s)"
 
 
+FP8_PER_BF16 = 2.0  # nominal dense tensor rate ratio (4.5 vs 2.25 PFLOP/s per GPU)
+FLOP_PER_ROW_POSITION = 2 * 576 + 2 * 512  # q . x over 576 dims, p * x over 512
+
+
+def algorithmic_flops(lens, T, H):
+    """Useful flops of one decode call: 2,176 per (query row, visible position);
+    query t of a request of length L sees L - T + 1 + t positions."""
+    return FLOP_PER_ROW_POSITION * H * sum(T * (L - T + 1) + T * (T - 1) // 2 for L in lens if L > 0)
+
+
+def tensor_roofline(flops, kernel_s):
+    """The decode kernel against the FP8 tensor peak: the measured bf16 burst peak
+    times the nominal fp8/bf16 ratio (the MMAs are e4m3 x e4m3)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            bf16 = float(json.load(f)["bf16_tflops"])
+        src = "measured bf16 burst (MEASURED_PEAKS.json bf16_tflops) x 2, the nominal fp8/bf16 ratio"
+    else:
+        bf16, src = 1900.0, "fallback bf16 1.9 PFLOP/s x 2, the nominal fp8/bf16 ratio"
+    peak = bf16 * FP8_PER_BF16
+    achieved = flops / kernel_s / 1e12
+    return {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4), "peak_source": src, "algorithmic_flops_per_launch": flops,
+            "note": "algorithmic flops (2,176 per row and visible position); the kernel issues twice "
+                    "that on the tensor cores (two-term query and probability splits)"}
+
+
 def carve(device, specs, pin=False):
     """One byte buffer holding a tensor per (shape, dtype) at 256-byte aligned
     offsets; returns the buffer and the typed views."""
@@ -348,6 +376,9 @@ def run_ours(args):
                 "kernel_p90_us": round(kernel_ms[(9 * len(kernel_ms)) // 10] * 1e3, 2),
                 "frac_of_8TBps": round(achieved / HBM_NOMINAL_GBS, 4),
                 "algorithmic_bytes_per_launch": kv_bytes}
+    # the many-row shapes are real contractions: their tensor-core side as well
+    roofline_tensor = (tensor_roofline(algorithmic_flops(base.lens, T, H), k_avg_ms * 1e-3)
+                       if H * T > 16 and family == "tcgen05" else None)
 
     # ---- the ceiling of this access pattern: the same pages, no arithmetic ----
     ceiling = None
@@ -538,6 +569,7 @@ def run_ours(args):
                                if rep_us else None),
             "frac_of_8TBps": round(value / HBM_NOMINAL_GBS, 4),
             "roofline": roofline,
+            "roofline_tensor": roofline_tensor,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "stream_ceiling": ceiling,

@@ -54,3 +54,19 @@ def test_parity_of_applies_the_tolerances():
     o4 = o.copy()
     o4[0, 0, 0, 0] = np.nan
     assert not bench.parity_of(o4, l, ro, rl)["pass"]
+
+
+def test_algorithmic_flops_counts_visible_positions():
+    # T = 1: every row sees the whole history
+    assert bench.algorithmic_flops([100, 0, 64], 1, 12) == 2176 * 12 * 164
+    # causal verify: query t of a length-L request sees L - T + 1 + t positions
+    lens, T, H = [50, 7], 4, 3
+    brute = sum(2176 * H * (L - T + 1 + t) for L in lens for t in range(T))
+    assert bench.algorithmic_flops(lens, T, H) == brute
+
+
+def test_tensor_roofline_fields():
+    r = bench.tensor_roofline(1e12, 1e-3)  # 1 TFLOP in 1 ms
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert abs(r["achieved"] - 1000.0) < 1e-6
+    assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-3
