@@ -52,6 +52,14 @@
 #include <stddef.h>
 #include <stdint.h>
 
+/* Every entry point carries MLA_API: the library is built with hidden symbol
+ * visibility, so these declarations are its only exported names. */
+#if defined(__GNUC__) || defined(__clang__)
+#define MLA_API __attribute__((visibility("default")))
+#else
+#define MLA_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -126,7 +134,7 @@ typedef enum {
  * device error 2; a seq_len outside [0, 64 * max_pages], or in (0, T), is
  * treated as 0 and sets device error 3 (see mla_device_error).
  */
-mla_status_t mla_decode_paged(const mla_tensor_t *q, const mla_tensor_t *kv_cache,
+MLA_API mla_status_t mla_decode_paged(const mla_tensor_t *q, const mla_tensor_t *kv_cache,
                               const float *kv_scale, const mla_tensor_t *block_table,
                               const mla_tensor_t *seq_lens, int32_t n_splits, float sm_scale,
                               const mla_tensor_t *out, const mla_tensor_t *lse, void *stream);
@@ -147,7 +155,7 @@ mla_status_t mla_decode_paged(const mla_tensor_t *q, const mla_tensor_t *kv_cach
  *   out         bf16 [B, T, H, 512], device, contiguous.
  *   lse         fp32 [B, T, H], device, contiguous, or NULL.
  */
-mla_status_t mla_merge_partials(const mla_tensor_t *partial_out, const mla_tensor_t *partial_lse,
+MLA_API mla_status_t mla_merge_partials(const mla_tensor_t *partial_out, const mla_tensor_t *partial_lse,
                                 int32_t n_shards, const mla_tensor_t *out,
                                 const mla_tensor_t *lse, void *stream);
 
@@ -171,7 +179,7 @@ mla_status_t mla_merge_partials(const mla_tensor_t *partial_out, const mla_tenso
  * it keeps the previous call's contents (nothing in it needs to start at
  * zero): calls that overlap on the GPU, on any streams, race with each other.
  */
-mla_status_t mla_decode_paged_noalloc(const mla_tensor_t *q, const mla_tensor_t *kv_cache,
+MLA_API mla_status_t mla_decode_paged_noalloc(const mla_tensor_t *q, const mla_tensor_t *kv_cache,
                                       const float *kv_scale, const mla_tensor_t *block_table,
                                       const mla_tensor_t *seq_lens, int32_t n_splits,
                                       float sm_scale, const mla_tensor_t *out,
@@ -205,7 +213,7 @@ mla_status_t mla_decode_paged_noalloc(const mla_tensor_t *q, const mla_tensor_t 
  * Returns MLA_OK or an error status (nothing is launched on error); B*T = 0
  * is a no-op.  The call allocates nothing and never synchronises.
  */
-mla_status_t mla_append_latent(const mla_tensor_t *latent, const float *kv_scale,
+MLA_API mla_status_t mla_append_latent(const mla_tensor_t *latent, const float *kv_scale,
                                const mla_tensor_t *block_table, const mla_tensor_t *start_pos,
                                const mla_tensor_t *kv_cache, void *stream);
 
@@ -219,7 +227,7 @@ mla_status_t mla_append_latent(const mla_tensor_t *latent, const float *kv_scale
  * (10,240 positions), so that in a batch of mixed lengths the longest request
  * does not bound the call.
  * Pure host function; sm_count <= 0 means "query the current device". */
-int32_t mla_auto_splits(int32_t B, int32_t T, int32_t H, int32_t max_pages, int32_t sm_count);
+MLA_API int32_t mla_auto_splits(int32_t B, int32_t T, int32_t H, int32_t max_pages, int32_t sm_count);
 
 /* The split count for a batch whose lengths the caller knows on the host (a
  * serving engine schedules them): pass the result as n_splits.  For units of
@@ -236,40 +244,40 @@ int32_t mla_auto_splits(int32_t B, int32_t T, int32_t H, int32_t max_pages, int3
  *                  seq_lens (values outside [0, 64 * max_pages] are clamped).
  *   max_pages      the block table's width, as passed to the decode.
  * Pure host function; sm_count <= 0 means "query the current device". */
-int32_t mla_plan_splits(int32_t B, int32_t T, int32_t H, const int32_t *host_seq_lens,
+MLA_API int32_t mla_plan_splits(int32_t B, int32_t T, int32_t H, const int32_t *host_seq_lens,
                         int32_t max_pages, int32_t sm_count);
 
 /* Pages per partition for a given split count: ceil(max_pages / n_splits),
  * so that the partitions of a full-length request differ by at most one
  * page, except the last, which takes the remainder. */
-int32_t mla_split_chunk_pages(int32_t max_pages, int32_t n_splits);
+MLA_API int32_t mla_split_chunk_pages(int32_t max_pages, int32_t n_splits);
 
 /* Bytes of library scratch one mla_decode_paged call with these sizes uses
  * (0 when n_splits resolves to 1). */
-size_t mla_decode_workspace_bytes(int32_t B, int32_t T, int32_t H, int32_t n_splits);
+MLA_API size_t mla_decode_workspace_bytes(int32_t B, int32_t T, int32_t H, int32_t n_splits);
 
 /* Select the kernel family for subsequent mla_decode_paged calls in this
  * process (all threads).  Returns the previous setting. */
-int32_t mla_set_impl(int32_t impl);
+MLA_API int32_t mla_set_impl(int32_t impl);
 
 /* Kernel family (MLA_IMPL_SIMT or MLA_IMPL_TCGEN05) that the calling thread's
  * last successful mla_decode_paged call launched; 0 before any call. */
-int32_t mla_last_decode_impl(void);
+MLA_API int32_t mla_last_decode_impl(void);
 
 /* Synchronise `stream`, then read and clear the device error word of the
  * current device: 0 means no kernel reported an error.  Codes: 1 a bounded
  * wait timed out, 2 a page id out of range, 3 a seq_len out of range. */
-mla_status_t mla_device_error(int32_t *code, void *stream);
+MLA_API mla_status_t mla_device_error(int32_t *code, void *stream);
 
 /* Benchmark instrumentation: the next mla_decode_paged call made by the
  * calling thread records ev_begin on its stream just before its split-KV
  * kernel and ev_end just after that kernel (before the split combine).  The
  * events are cudaEvent_t handles passed as void*; either may be NULL.  The
  * request is one-shot and thread-local; it changes nothing else. */
-mla_status_t mla_profile_next_decode(void *ev_begin, void *ev_end);
+MLA_API mla_status_t mla_profile_next_decode(void *ev_begin, void *ev_end);
 
-const char *mla_status_string(mla_status_t status);
-const char *mla_last_error(void);   /* thread-local; "" when none */
+MLA_API const char *mla_status_string(mla_status_t status);
+MLA_API const char *mla_last_error(void);   /* thread-local; "" when none */
 
 #ifdef __cplusplus
 }

@@ -13,6 +13,8 @@
 
 #include <stdint.h>
 
+#include "mla_decode.h" /* MLA_API */
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -22,7 +24,7 @@ extern "C" {
  * after 2 s and the launch ends with device error 1; its outputs are
  * undefined.  on == 0 restores normal operation.  Returns the previous
  * setting.  Host-side only: nothing on the GPU faults, traps or hangs. */
-int mla_test_stall_copies(int on);
+MLA_API int mla_test_stall_copies(int on);
 
 /* Benchmark instrumentation: the HBM ceiling of the decode's access pattern.
  * Launches `ctas` CTAs; CTA c copies the pages page_ids[c * pages_per_cta + i]
@@ -40,7 +42,7 @@ int mla_test_stall_copies(int on);
  * Asynchronous on `stream`; returns an mla_status_t (0 = MLA_OK; nothing is
  * launched on error).  Waits are bounded like the decode kernel's (2 s,
  * device error 1). */
-int mla_bench_stream_pages(const void *kv_cache, int64_t num_pages, const int32_t *page_ids,
+MLA_API int mla_bench_stream_pages(const void *kv_cache, int64_t num_pages, const int32_t *page_ids,
                            int32_t ctas, int32_t pages_per_cta, void *stream);
 
 #ifdef __cplusplus

@@ -27,8 +27,9 @@ def _nvcc():
 
 
 def _flags(verbose_ptxas: bool):
+    # hidden visibility: only the MLA_API entry points of include/*.h are exported
     f = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
-         "--expt-relaxed-constexpr", *ARCH]
+         "-Xcompiler", "-fvisibility=hidden", "--expt-relaxed-constexpr", *ARCH]
     if verbose_ptxas:
         f += ["-Xptxas", "-v"]
     return f

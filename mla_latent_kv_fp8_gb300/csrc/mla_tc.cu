@@ -51,6 +51,7 @@
 #include <atomic>
 #include <mutex>
 
+#include "../../include/mla_decode_testing.h"
 #include "mla_internal.cuh"
 #include "mla_tc_ptx.cuh"
 

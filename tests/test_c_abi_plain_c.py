@@ -70,3 +70,23 @@ def test_plain_c_program_calls_the_library(built):
     assert int(chunk) == 27
     assert int(ws) == _lib.mla_decode_workspace_bytes(8, 1, 12, 19)
     assert msg.strip() == _lib.mla_status_string(1)
+
+
+def test_library_exports_only_the_declared_entry_points():
+    """Built with hidden visibility: the defined functions the library exports are
+    exactly the MLA_API declarations of include/*.h (the C++ internals stay
+    private; weak C++ standard-library instantiations are not functions of ours)."""
+    import re
+    if shutil.which("nm") is None:
+        pytest.skip("no nm")
+    so = os.path.join(PKG, "libmla_decode.so")
+    if not os.path.exists(so):
+        from mla_latent_kv_fp8_gb300 import build
+        build.build()
+    declared = set()
+    for h in os.listdir(INC):
+        if h.endswith(".h"):
+            declared |= set(re.findall(r"^MLA_API [^(]*?\b(mla_\w+)\(", open(os.path.join(INC, h)).read(), re.M))
+    out = subprocess.run(["nm", "-D", "--defined-only", so], check=True, capture_output=True, text=True).stdout
+    exported = {parts[2] for parts in (ln.split() for ln in out.splitlines()) if len(parts) == 3 and parts[1] == "T"}
+    assert declared and exported == declared, (sorted(exported - declared), sorted(declared - exported))
