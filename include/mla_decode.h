@@ -35,9 +35,11 @@
  * CUDA graphs: a call may be captured once an uncaptured call of at least
  * the same scratch size has run on that stream; a captured call that would
  * have to grow the scratch returns MLA_ERR_UNSUPPORTED and records nothing.
- * Scratch that a captured call used is never freed, so the graph stays valid
- * after later, larger calls on the stream; a graph replayed on another stream
- * still uses the scratch of the stream it was captured on.
+ * Scratch that a captured call used is not freed when the stream's scratch
+ * grows, so the graph stays valid after later, larger calls on the stream; a
+ * graph replayed on another stream still uses the scratch of the stream it was
+ * captured on.  mla_release_graph_scratch() frees such scratch once the graphs
+ * that used it are gone.
  *
  * Errors: every entry point validates its arguments on the host before any
  * launch and returns a status; mla_last_error() gives a message for the last
@@ -101,8 +103,9 @@ typedef enum {
  * mla_decode_paged -- MLA decode attention over a paged FP8 latent cache,
  * split into n_splits parallel partitions of the history and merged by LSE.
  *
- *   q           bf16  [B, T, H, 576], device, innermost dim contiguous; the
- *               absorbed, already-rotated query of each head.
+ *   q           bf16  [B, T, H, 576], device, fully contiguous, base address
+ *               16-byte aligned; the absorbed, already-rotated query of each
+ *               head.
  *   kv_cache    e4m3fn [num_pages, 64, 576], device, fully contiguous; base
  *               address 16-byte aligned.
  *   kv_scale    device pointer to one fp32, the per-tensor dequantisation
@@ -171,9 +174,14 @@ MLA_API mla_status_t mla_merge_partials(const mla_tensor_t *partial_out, const m
  * The split partials live in one fixed device array of 8 MiB inside the
  * library (every GPU that loads the library holds it until the process
  * exits); this call never calls cudaMalloc, cudaMallocAsync or cudaFree.
- * A call whose partials need more than 8 MiB (see
- * mla_decode_workspace_bytes) returns MLA_ERR_UNSUPPORTED with a message and
- * launches nothing; pass a smaller n_splits.  The first call on each device
+ * With n_splits = 0 the automatic count (mla_auto_splits) is capped at the
+ * largest count whose partials fit 8 MiB, down to 1 (no split, no scratch),
+ * so the automatic mode always runs.  An explicit n_splits whose partials need
+ * more than 8 MiB (see mla_decode_workspace_bytes) returns
+ * MLA_ERR_UNSUPPORTED with a message and launches nothing.  Kernel family,
+ * profile events and test hooks apply as for mla_decode_paged.  The library
+ * does not survive cudaDeviceReset (the array's cached address would be
+ * stale).  The first call on each device
  * looks up the array's device address with that device current; make that
  * first call before any stream capture.  All calls share the one array and
  * it keeps the previous call's contents (nothing in it needs to start at
@@ -255,6 +263,14 @@ MLA_API int32_t mla_split_chunk_pages(int32_t max_pages, int32_t n_splits);
 /* Bytes of library scratch one mla_decode_paged call with these sizes uses
  * (0 when n_splits resolves to 1). */
 MLA_API size_t mla_decode_workspace_bytes(int32_t B, int32_t T, int32_t H, int32_t n_splits);
+
+/* Free the split scratch that calls captured in CUDA graphs used (on the
+ * current device): the buffers kept when a stream's scratch grew, and the
+ * live buffers of streams whose calls were captured (their next uncaptured
+ * call allocates anew).  Call it only when no graph that captured a library
+ * call on this device will be replayed again (e.g. after destroying them).
+ * Synchronises the device (cudaFree). */
+MLA_API mla_status_t mla_release_graph_scratch(void);
 
 /* Select the kernel family for subsequent mla_decode_paged calls in this
  * process (all threads).  Returns the previous setting. */

@@ -19,12 +19,24 @@
 extern "C" {
 #endif
 
-/* on != 0: every later tensor-core decode launch (from any thread, on any
- * device) issues no page copies, so each of its waits for a page runs out
- * after 2 s and the launch ends with device error 1; its outputs are
- * undefined.  on == 0 restores normal operation.  Returns the previous
- * setting.  Host-side only: nothing on the GPU faults, traps or hangs. */
+/* on != 0: every later tensor-core decode launch made from the CALLING
+ * THREAD (other threads are unaffected) issues no page copies, so each of its
+ * waits for a page runs out after 2 s and the launch ends with device error
+ * 1; its outputs are undefined.  on == 0 restores normal operation.  Returns
+ * the previous setting of this thread.  Host-side only: nothing on the GPU
+ * faults, traps or hangs. */
 MLA_API int mla_test_stall_copies(int on);
+
+/* Instrumentation of the tensor-core kernels' online softmax: the next decode
+ * call (mla_decode_paged or mla_decode_paged_noalloc) made by the calling
+ * thread adds, with device atomics, to device_counts[0] the number of times an
+ * attention warpgroup rescaled its accumulated output tile in tensor memory
+ * because a row's reference maximum moved after that warpgroup's first page,
+ * and to device_counts[1] the number of reference moves of any kind
+ * (including the first page's).  device_counts: device int32[2], zeroed by the
+ * caller.  One-shot and thread-local; the CUDA-core kernel counts nothing.
+ * Returns 0. */
+MLA_API int mla_test_count_rescales(int32_t *device_counts);
 
 /* Benchmark instrumentation: the HBM ceiling of the decode's access pattern.
  * Launches `ctas` CTAs; CTA c copies the pages page_ids[c * pages_per_cta + i]

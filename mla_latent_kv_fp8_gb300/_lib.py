@@ -29,7 +29,8 @@ EXPORTS = ("mla_decode_paged", "mla_merge_partials", "mla_auto_splits", "mla_spl
            "mla_decode_workspace_bytes", "mla_set_impl", "mla_device_error", "mla_status_string",
            "mla_last_error", "mla_profile_next_decode", "mla_last_decode_impl",
            "mla_decode_paged_noalloc", "mla_test_stall_copies", "mla_bench_stream_pages",
-           "mla_append_latent", "mla_plan_splits")
+           "mla_append_latent", "mla_plan_splits", "mla_test_count_rescales",
+           "mla_release_graph_scratch")
 
 
 class MlaError(RuntimeError):
@@ -71,6 +72,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mla_set_impl.restype = ctypes.c_int32
     lib.mla_test_stall_copies.argtypes = [ctypes.c_int]
     lib.mla_test_stall_copies.restype = ctypes.c_int
+    lib.mla_test_count_rescales.argtypes = [P]
+    lib.mla_test_count_rescales.restype = ctypes.c_int
+    lib.mla_release_graph_scratch.argtypes = []
+    lib.mla_release_graph_scratch.restype = ctypes.c_int
     lib.mla_bench_stream_pages.argtypes = [P, ctypes.c_int64, P, ctypes.c_int32, ctypes.c_int32, P]
     lib.mla_bench_stream_pages.restype = ctypes.c_int
     lib.mla_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32), P]
@@ -188,10 +193,23 @@ def mla_set_impl(impl: int) -> int:
 
 
 def mla_test_stall_copies(on: bool) -> int:
-    """Failure-detection tests only: later tensor-core launches issue no page
-    copies, so their bounded waits run out (device error 1).  Returns the
-    previous setting."""
+    """Failure-detection tests only: later tensor-core launches from this thread
+    issue no page copies, so their bounded waits run out (device error 1).
+    Returns the previous setting of this thread."""
     return lib().mla_test_stall_copies(1 if on else 0)
+
+
+def mla_test_count_rescales(device_counts):
+    """The next decode call of this thread adds to device_counts (a zeroed int32
+    CUDA tensor of 2): [0] in-place rescales of accumulated output tiles after a
+    warpgroup's first page, [1] reference moves of any kind."""
+    _check(lib().mla_test_count_rescales(ctypes.c_void_p(device_counts.data_ptr())))
+
+
+def mla_release_graph_scratch():
+    """Free the split scratch kept for captured CUDA graphs on the current device
+    (only once no such graph will be replayed)."""
+    _check(lib().mla_release_graph_scratch())
 
 
 def mla_bench_stream_pages(kv_cache, page_ids, ctas, pages_per_cta, stream=None):

@@ -16,6 +16,7 @@
 
 #include "../../include/mla_decode.h"
 #include "../../include/mla_decode_testing.h"
+#include "mla_host.h"
 #include "mla_internal.cuh"
 
 // The device error word written by kernels (bounded waits, bounds checks).
@@ -23,14 +24,15 @@ __device__ int g_mla_device_error;
 
 namespace mla {
 
-cudaError_t launch_tc_decode(const DecodeParams& p, cudaStream_t stream, bool* handled);
-
 namespace {
 
 thread_local std::string t_last_error;
 thread_local cudaEvent_t t_prof_begin = nullptr;
 thread_local cudaEvent_t t_prof_end = nullptr;
 thread_local int t_last_impl = 0;
+// Test hooks (include/mla_decode_testing.h): per calling thread.
+thread_local int* t_test_counts = nullptr;  // one-shot: the next decode call only
+thread_local int t_test_stall = 0;
 std::atomic<int> g_impl{MLA_IMPL_AUTO};
 
 mla_status_t fail(mla_status_t st, const char* fmt, ...) {
@@ -90,7 +92,9 @@ struct Scratch {
 };
 std::mutex g_ws_mu;
 std::map<std::pair<int, void*>, Scratch> g_ws;
-std::vector<void*> g_ws_retired;  // kept for the graphs that may still use them
+// Buffers a captured call used, kept (with their device) for the graphs that
+// may still replay them, until mla_release_graph_scratch.
+std::vector<std::pair<int, void*>> g_ws_retired;
 
 mla_status_t get_scratch(size_t need, cudaStream_t stream, void** out) {
     *out = nullptr;
@@ -113,7 +117,7 @@ mla_status_t get_scratch(size_t need, cudaStream_t stream, void** out) {
                         need);
         if (s.ptr) {
             if (s.in_graph) {
-                g_ws_retired.push_back(s.ptr);
+                g_ws_retired.push_back({dev, s.ptr});
             } else {
                 e = cudaFreeAsync(s.ptr, stream);
                 if (e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync(scratch)");
@@ -167,11 +171,10 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 }  // namespace
 
-// Accessors for the library's other host translation units.
+// Accessors for the library's other host translation units (mla_host.h).
 mla_status_t internal_fail(mla_status_t st, const char* msg) { return fail(st, "%s", msg); }
 mla_status_t internal_cuda_fail(cudaError_t e, const char* what) { return cuda_fail(e, what); }
 void internal_clear_error() { t_last_error.clear(); }
-void internal_set_last_impl(int impl) { t_last_impl = impl; }
 mla_status_t internal_device(int** err_word, int* sm_count) {
     DeviceInfo* d = nullptr;
     mla_status_t st = device_info(&d);
@@ -183,6 +186,121 @@ mla_status_t internal_device(int** err_word, int* sm_count) {
 mla_status_t internal_check_tensor(const mla_tensor_t* t, const char* name, int ndim, int dtype,
                                    bool need_contig, size_t align) {
     return check_tensor(t, name, ndim, dtype, need_contig, align);
+}
+
+mla_status_t internal_prepare_decode(const mla_tensor_t* q, const mla_tensor_t* kv_cache, const float* kv_scale,
+                                     const mla_tensor_t* block_table, const mla_tensor_t* seq_lens,
+                                     int32_t n_splits, int32_t auto_splits_cap, float sm_scale,
+                                     const mla_tensor_t* out, const mla_tensor_t* lse, DecodeParams* pp,
+                                     bool* empty) {
+    *empty = false;
+    mla_status_t st;
+    if ((st = check_tensor(q, "q", 4, MLA_DTYPE_BF16, true, 16)) != MLA_OK) return st;
+    const int64_t B = q->shape[0], T = q->shape[1], H = q->shape[2];
+    if (q->shape[3] != kDqk) return fail(MLA_ERR_UNSUPPORTED, "q: last dim %lld, only 576 is supported", (long long)q->shape[3]);
+    if (T < 1 || H < 1) return fail(MLA_ERR_INVALID_ARG, "q: T and H must be >= 1");
+    if (H * T > kMaxRows) return fail(MLA_ERR_UNSUPPORTED, "H*T = %lld exceeds %d", (long long)(H * T), kMaxRows);
+    if ((st = check_tensor(kv_cache, "kv_cache", 3, MLA_DTYPE_E4M3FN, true, 16)) != MLA_OK) return st;
+    if (kv_cache->shape[1] != kPage || kv_cache->shape[2] != kDqk)
+        return fail(MLA_ERR_UNSUPPORTED, "kv_cache: must be [num_pages, 64, 576]");
+    if (!kv_scale) return fail(MLA_ERR_INVALID_ARG, "kv_scale: null pointer");
+    if ((st = check_tensor(block_table, "block_table", 2, MLA_DTYPE_I32, false, 4)) != MLA_OK) return st;
+    if (block_table->shape[0] != B) return fail(MLA_ERR_INVALID_ARG, "block_table: first dim must be B");
+    const int64_t max_pages = block_table->shape[1];
+    if (block_table->stride[1] != 1 || block_table->stride[0] < max_pages)
+        return fail(MLA_ERR_UNSUPPORTED, "block_table: rows must be contiguous");
+    if ((st = check_tensor(seq_lens, "seq_lens", 1, MLA_DTYPE_I32, true, 4)) != MLA_OK) return st;
+    if (seq_lens->shape[0] != B) return fail(MLA_ERR_INVALID_ARG, "seq_lens: must have B entries");
+    if ((st = check_tensor(out, "out", 4, MLA_DTYPE_BF16, true, 16)) != MLA_OK) return st;
+    if (out->shape[0] != B || out->shape[1] != T || out->shape[2] != H || out->shape[3] != kDv)
+        return fail(MLA_ERR_INVALID_ARG, "out: must be [B, T, H, 512]");
+    if (lse) {
+        if ((st = check_tensor(lse, "lse", 3, MLA_DTYPE_F32, true, 4)) != MLA_OK) return st;
+        if (lse->shape[0] != B || lse->shape[1] != T || lse->shape[2] != H)
+            return fail(MLA_ERR_INVALID_ARG, "lse: must be [B, T, H]");
+    }
+    if (n_splits < 0) return fail(MLA_ERR_INVALID_ARG, "n_splits must be >= 0");
+    if (max_pages < 1 && B > 0) return fail(MLA_ERR_INVALID_ARG, "block_table: needs >= 1 column");
+    if (max_pages > (1 << 24)) return fail(MLA_ERR_UNSUPPORTED, "block_table: more than 2^24 pages per request");
+    if (B > 65535) return fail(MLA_ERR_UNSUPPORTED, "B > 65535");
+    if (B == 0) {
+        *empty = true;
+        return MLA_OK;
+    }
+
+    DeviceInfo* dev = nullptr;
+    if ((st = device_info(&dev)) != MLA_OK) return st;
+
+    int32_t req = n_splits;
+    if (req == 0) {
+        req = mla_auto_splits((int32_t)B, (int32_t)T, (int32_t)H, (int32_t)max_pages, dev->sm_count);
+        if (auto_splits_cap > 0 && req > auto_splits_cap) req = auto_splits_cap;
+    }
+    const int32_t chunk = mla_split_chunk_pages((int32_t)max_pages, req);
+    const int32_t n_eff = (int32_t)ceil_div(max_pages, chunk);
+
+    DecodeParams p{};
+    p.q = static_cast<const uint16_t*>(q->data);
+    p.kv = static_cast<const uint8_t*>(kv_cache->data);
+    p.kv_scale = kv_scale;
+    p.block_table = static_cast<const int32_t*>(block_table->data);
+    p.seq_lens = static_cast<const int32_t*>(seq_lens->data);
+    p.bt_stride = block_table->stride[0];
+    p.num_pages = kv_cache->shape[0];
+    p.B = (int)B;
+    p.T = (int)T;
+    p.H = (int)H;
+    p.max_pages = (int)max_pages;
+    p.n_splits = n_eff;
+    p.chunk_pages = chunk;
+    p.sm_scale_log2 = sm_scale * kLog2e;
+    p.out = static_cast<uint16_t*>(out->data);
+    p.lse = lse ? static_cast<float*>(lse->data) : nullptr;
+    p.err = dev->err_word;
+    *pp = p;
+    return MLA_OK;
+}
+
+mla_status_t internal_launch_decode(DecodeParams& p, cudaStream_t s) {
+    // the calling thread's one-shot requests apply to this call only
+    cudaEvent_t ev_begin = t_prof_begin, ev_end = t_prof_end;
+    t_prof_begin = t_prof_end = nullptr;
+    p.test_counts = t_test_counts;
+    t_test_counts = nullptr;
+    p.test_stall_copies = t_test_stall;
+
+    const int impl = g_impl.load();
+    cudaError_t e = cudaSuccess;
+    bool handled = false;
+    if (ev_begin && (e = cudaEventRecord(ev_begin, s)) != cudaSuccess)
+        return cuda_fail(e, "cudaEventRecord(profile begin)");
+    if (impl == MLA_IMPL_AUTO || impl == MLA_IMPL_TCGEN05) {
+        e = launch_tc_decode(p, s, &handled);
+        if (e != cudaSuccess) return cuda_fail(e, "tcgen05 decode launch");
+        if (!handled && impl == MLA_IMPL_TCGEN05)
+            return fail(MLA_ERR_UNSUPPORTED, "tcgen05 kernel does not support this shape");
+    }
+    if (!handled) {
+        e = launch_simt_decode(p, s);
+        if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    }
+    t_last_impl = handled ? MLA_IMPL_TCGEN05 : MLA_IMPL_SIMT;
+    if (ev_end && (e = cudaEventRecord(ev_end, s)) != cudaSuccess)
+        return cuda_fail(e, "cudaEventRecord(profile end)");
+    if (p.n_splits > 1) {
+        MergeParams m{};
+        m.part_out = p.part_out;
+        m.part_lse = p.part_lse;
+        m.S = p.n_splits;
+        m.rows = (int64_t)p.B * p.T * p.H;
+        m.in_bf16 = 0;
+        m.out = p.out;
+        m.lse = p.lse;
+        m.pdl = 1;
+        e = launch_merge(m, s);
+        if (e != cudaSuccess) return cuda_fail(e, "split combine launch");
+    }
+    return MLA_OK;
 }
 
 }  // namespace mla
@@ -367,114 +485,69 @@ mla_status_t mla_decode_paged(const mla_tensor_t* q, const mla_tensor_t* kv_cach
                               const mla_tensor_t* seq_lens, int32_t n_splits, float sm_scale,
                               const mla_tensor_t* out, const mla_tensor_t* lse, void* stream) {
     t_last_error.clear();
-    mla_status_t st;
-    if ((st = check_tensor(q, "q", 4, MLA_DTYPE_BF16, true, 16)) != MLA_OK) return st;
-    const int64_t B = q->shape[0], T = q->shape[1], H = q->shape[2];
-    if (q->shape[3] != kDqk) return fail(MLA_ERR_UNSUPPORTED, "q: last dim %lld, only 576 is supported", (long long)q->shape[3]);
-    if (T < 1 || H < 1) return fail(MLA_ERR_INVALID_ARG, "q: T and H must be >= 1");
-    if (H * T > kMaxRows) return fail(MLA_ERR_UNSUPPORTED, "H*T = %lld exceeds %d", (long long)(H * T), kMaxRows);
-    if ((st = check_tensor(kv_cache, "kv_cache", 3, MLA_DTYPE_E4M3FN, true, 16)) != MLA_OK) return st;
-    if (kv_cache->shape[1] != kPage || kv_cache->shape[2] != kDqk)
-        return fail(MLA_ERR_UNSUPPORTED, "kv_cache: must be [num_pages, 64, 576]");
-    if (!kv_scale) return fail(MLA_ERR_INVALID_ARG, "kv_scale: null pointer");
-    if ((st = check_tensor(block_table, "block_table", 2, MLA_DTYPE_I32, false, 4)) != MLA_OK) return st;
-    if (block_table->shape[0] != B) return fail(MLA_ERR_INVALID_ARG, "block_table: first dim must be B");
-    const int64_t max_pages = block_table->shape[1];
-    if (block_table->stride[1] != 1 || block_table->stride[0] < max_pages)
-        return fail(MLA_ERR_UNSUPPORTED, "block_table: rows must be contiguous");
-    if ((st = check_tensor(seq_lens, "seq_lens", 1, MLA_DTYPE_I32, true, 4)) != MLA_OK) return st;
-    if (seq_lens->shape[0] != B) return fail(MLA_ERR_INVALID_ARG, "seq_lens: must have B entries");
-    if ((st = check_tensor(out, "out", 4, MLA_DTYPE_BF16, true, 16)) != MLA_OK) return st;
-    if (out->shape[0] != B || out->shape[1] != T || out->shape[2] != H || out->shape[3] != kDv)
-        return fail(MLA_ERR_INVALID_ARG, "out: must be [B, T, H, 512]");
-    if (lse) {
-        if ((st = check_tensor(lse, "lse", 3, MLA_DTYPE_F32, true, 4)) != MLA_OK) return st;
-        if (lse->shape[0] != B || lse->shape[1] != T || lse->shape[2] != H)
-            return fail(MLA_ERR_INVALID_ARG, "lse: must be [B, T, H]");
-    }
-    if (n_splits < 0) return fail(MLA_ERR_INVALID_ARG, "n_splits must be >= 0");
-    if (max_pages < 1 && B > 0) return fail(MLA_ERR_INVALID_ARG, "block_table: needs >= 1 column");
-    if (max_pages > (1 << 24)) return fail(MLA_ERR_UNSUPPORTED, "block_table: more than 2^24 pages per request");
-    if (B > 65535) return fail(MLA_ERR_UNSUPPORTED, "B > 65535");
-    if (B == 0) return MLA_OK;
-
-    DeviceInfo* dev = nullptr;
-    if ((st = device_info(&dev)) != MLA_OK) return st;
-
-    const int32_t req = n_splits > 0 ? n_splits
-                                     : mla_auto_splits((int32_t)B, (int32_t)T, (int32_t)H,
-                                                       (int32_t)max_pages, dev->sm_count);
-    const int32_t chunk = mla_split_chunk_pages((int32_t)max_pages, req);
-    const int32_t n_eff = (int32_t)ceil_div(max_pages, chunk);
-
     DecodeParams p{};
-    p.q = static_cast<const uint16_t*>(q->data);
-    p.kv = static_cast<const uint8_t*>(kv_cache->data);
-    p.kv_scale = kv_scale;
-    p.block_table = static_cast<const int32_t*>(block_table->data);
-    p.seq_lens = static_cast<const int32_t*>(seq_lens->data);
-    p.bt_stride = block_table->stride[0];
-    p.num_pages = kv_cache->shape[0];
-    p.B = (int)B;
-    p.T = (int)T;
-    p.H = (int)H;
-    p.max_pages = (int)max_pages;
-    p.n_splits = n_eff;
-    p.chunk_pages = chunk;
-    p.sm_scale_log2 = sm_scale * kLog2e;
-    p.out = static_cast<uint16_t*>(out->data);
-    p.lse = lse ? static_cast<float*>(lse->data) : nullptr;
-    p.err = dev->err_word;
-
+    bool empty = false;
+    mla_status_t st = internal_prepare_decode(q, kv_cache, kv_scale, block_table, seq_lens, n_splits, 0,
+                                              sm_scale, out, lse, &p, &empty);
+    if (st != MLA_OK || empty) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (n_eff > 1) {
+    if (p.n_splits > 1) {
         void* ws = nullptr;
-        const size_t need = mla_decode_workspace_bytes((int32_t)B, (int32_t)T, (int32_t)H, n_eff);
+        const size_t need = mla_decode_workspace_bytes(p.B, p.T, p.H, p.n_splits);
         if ((st = get_scratch(need, s, &ws)) != MLA_OK) return st;
-        const size_t out_bytes = (size_t)n_eff * B * T * H * kDv * sizeof(float);
+        const size_t out_bytes = (size_t)p.n_splits * p.B * p.T * p.H * kDv * sizeof(float);
         p.part_out = static_cast<float*>(ws);
         p.part_lse = reinterpret_cast<float*>(static_cast<char*>(ws) + ((out_bytes + 255) & ~size_t(255)));
     }
-
-    const int impl = g_impl.load();
-    cudaError_t e = cudaSuccess;
-    bool handled = false;
-    cudaEvent_t ev_begin = t_prof_begin, ev_end = t_prof_end;
-    t_prof_begin = t_prof_end = nullptr;
-    if (ev_begin && (e = cudaEventRecord(ev_begin, s)) != cudaSuccess)
-        return cuda_fail(e, "cudaEventRecord(profile begin)");
-    if (impl == MLA_IMPL_AUTO || impl == MLA_IMPL_TCGEN05) {
-        e = launch_tc_decode(p, s, &handled);
-        if (e != cudaSuccess) return cuda_fail(e, "tcgen05 decode launch");
-        if (!handled && impl == MLA_IMPL_TCGEN05)
-            return fail(MLA_ERR_UNSUPPORTED, "tcgen05 kernel does not support this shape");
-    }
-    if (!handled) {
-        e = launch_simt_decode(p, s);
-        if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-    }
-    t_last_impl = handled ? MLA_IMPL_TCGEN05 : MLA_IMPL_SIMT;
-    if (ev_end && (e = cudaEventRecord(ev_end, s)) != cudaSuccess)
-        return cuda_fail(e, "cudaEventRecord(profile end)");
-    if (n_eff > 1) {
-        MergeParams m{};
-        m.part_out = p.part_out;
-        m.part_lse = p.part_lse;
-        m.S = n_eff;
-        m.rows = B * T * H;
-        m.in_bf16 = 0;
-        m.out = p.out;
-        m.lse = p.lse;
-        m.pdl = 1;
-        e = launch_merge(m, s);
-        if (e != cudaSuccess) return cuda_fail(e, "split combine launch");
-    }
-    return MLA_OK;
+    return internal_launch_decode(p, s);
 }
 
 mla_status_t mla_profile_next_decode(void* ev_begin, void* ev_end) {
     t_prof_begin = static_cast<cudaEvent_t>(ev_begin);
     t_prof_end = static_cast<cudaEvent_t>(ev_end);
+    return MLA_OK;
+}
+
+mla_status_t mla_release_graph_scratch(void) {
+    t_last_error.clear();
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    // the current device's retired buffers, and the live buffers that a
+    // capture used (the next call on their stream allocates anew)
+    std::vector<void*> drop;
+    for (auto it = g_ws_retired.begin(); it != g_ws_retired.end();) {
+        if (it->first == dev) {
+            drop.push_back(it->second);
+            it = g_ws_retired.erase(it);
+        } else {
+            ++it;
+        }
+    }
+    for (auto& kv : g_ws) {
+        if (kv.first.first == dev && kv.second.in_graph && kv.second.ptr) {
+            drop.push_back(kv.second.ptr);
+            kv.second = Scratch{};
+        }
+    }
+    if (drop.empty()) return MLA_OK;
+    // cudaFree waits for the device; a buffer freed here is in no stream's use
+    for (void* ptr : drop) {
+        e = cudaFree(ptr);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFree(graph scratch)");
+    }
+    return MLA_OK;
+}
+
+int mla_test_stall_copies(int on) {
+    const int prev = t_test_stall;
+    t_test_stall = on ? 1 : 0;
+    return prev;
+}
+
+int mla_test_count_rescales(int32_t* device_counts) {
+    t_test_counts = device_counts;
     return MLA_OK;
 }
 

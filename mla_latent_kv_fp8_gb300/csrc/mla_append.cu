@@ -14,17 +14,9 @@
 // few KB per step; the kernel is launch-bound by design.
 #include <cuda_fp8.h>
 
-#include "../../include/mla_decode.h"
-#include "mla_internal.cuh"
+#include "mla_host.h"
 
 namespace mla {
-
-mla_status_t internal_fail(mla_status_t st, const char* msg);
-mla_status_t internal_cuda_fail(cudaError_t e, const char* what);
-void internal_clear_error();
-mla_status_t internal_device(int** err_word, int* sm_count);
-mla_status_t internal_check_tensor(const mla_tensor_t* t, const char* name, int ndim, int dtype,
-                                   bool need_contig, size_t align);
 
 namespace {
 

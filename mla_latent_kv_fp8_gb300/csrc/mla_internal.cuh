@@ -44,6 +44,10 @@ struct DecodeParams {
     float* part_lse;
     int* err;                   // device error word
     int test_stall_copies;      // failure-detection tests only: issue no page copies
+    // tests only (null otherwise): [0] += 1 each time an attention warpgroup
+    // rescales its accumulated output tile after a reference move past its
+    // first page, [1] += 1 for every reference move
+    int* test_counts;
     // tcgen05 kernel for more than 16 rows: CTAs per (partition, request) and
     // rows each (the last CTA may have fewer)
     int row_ctas;
@@ -62,6 +66,7 @@ struct MergeParams {
 };
 
 cudaError_t launch_simt_decode(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_tc_decode(const DecodeParams& p, cudaStream_t stream, bool* handled);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
 cudaError_t launch_stream_probe(const uint8_t* kv, int64_t num_pages, const int32_t* page_ids, int ctas,
                                 int pages_per_cta, int* err, cudaStream_t stream);
