@@ -25,6 +25,9 @@
 //     needed at the end.  Each lane works on 4 rows of one position.
 //   * PV: D[128 dims x 64] += V^T[128 x 64 pos] . [p1 | p2]^T per 128-dim block,
 //     P = p1 + p2 / 16 in e4m3 (relative error ~2^-8), 8 MMAs of N = 64 per page.
+//     A row's reference moves when a score would exceed it by 8 (log2 units)
+//     and then sits 7 below the page max, so the largest probability starts at
+//     2^7 and the e4m3 floor of tiny probabilities lies ~2^-21 below it.
 //   * TMEM: 2 score tiles x 128 columns + output 4 blocks x 64 columns = 512.
 // Warp roles (640 threads, one CTA per SM): warp 0 TMA producer (ring of 4
 // pages), warps 1 and 3 issue QK^T, warp 2 issues PV, warps 4-19 are the four
@@ -64,7 +67,7 @@ constexpr uint32_t kWSCols = 2 * kWN;        // 128: one score tile (K-half a | 
 constexpr uint32_t kWOCol0 = kWSBufs * kWSCols;  // 256: output tile, block c at + 64 c
 constexpr int kWSetupBar = 1 + kWGroups;     // named barrier of the set-up (warps 1..19)
 constexpr float kWHeadroom = 8.f;            // log2 units a score may exceed its row's reference
-constexpr float kWShift = 4.f;               // a new reference sits this far below the page max
+constexpr float kWShift = 7.f;               // a new reference sits this far below the page max
 static_assert(kWOCol0 + 4 * kWN <= kWTmemCols, "TMEM budget");
 // The probabilities of page i go to buffer i % kWPBufs, last read by the PV of
 // page i - kWPBufs.  With as many buffers as ring slots that PV has finished
@@ -539,6 +542,10 @@ __global__ void __launch_bounds__(kWThreads, 1)
                     const float rn = need ? t - kWShift : r_l;
                     const float a = need ? exp2f(r_l - rn) : 1.f;  // r_l = -inf: nothing to keep
                     r_l = rn;
+                    if (p.test_counts && quad == 0 && lane == 0) {
+                        atomicAdd(p.test_counts + 1, 1);
+                        if (i > 0) atomicAdd(p.test_counts, 1);
+                    }
 #pragma unroll
                     for (int j = 0; j < kWRL; ++j) {
                         rr[j] = __shfl_sync(0xffffffffu, rn, kWRL * half + j);
@@ -676,6 +683,8 @@ __global__ void __launch_bounds__(kWThreads, 1)
     }
 }
 }  // namespace
+
+// ---------------------------------------------------------------- host side
 
 // Launch the wide kernel: p.row_ctas CTAs per (partition, request), each of at
 // most 32 rows (p.rows_per_cta); the maps are those of the 12-head kernel

@@ -89,8 +89,18 @@ def _normal_chunk(seed_words, n, device):
     return torch.from_numpy(rng.standard_normal(n, dtype=np.float32))
 
 
-def _latent_codes(seed, lens_padded, device, scale=None):
-    """Per-request FP8 code blocks [Lpad_b, 576] for N(0,1) latents.
+def _latent_chunk(seed, b, c0, m, device, pattern):
+    """Latents of positions c0 .. c0+m-1 of request b, fp32 [m, 576]: N(0,1)
+    draws, reshaped by the stress pattern if one is given."""
+    x = _normal_chunk((seed, 7, b, c0), m * D_QK, device).view(m, D_QK)
+    if pattern is not None:
+        x = pattern.latents(b, c0, x)
+    return x
+
+
+def _latent_codes(seed, lens_padded, device, scale=None, pattern=None):
+    """Per-request FP8 code blocks [Lpad_b, 576] for N(0,1) latents (or the
+    latents of a stress pattern).
 
     Two passes over the same seed-addressed chunks: amax first (unless a scale
     is supplied), then quantisation.  Returns (list of uint8 tensors, scale)."""
@@ -99,8 +109,7 @@ def _latent_codes(seed, lens_padded, device, scale=None):
         amax = 0.0
         for b, L in enumerate(lens_padded):
             for c0 in range(0, L, chunk):
-                n = min(chunk, L - c0) * D_QK
-                x = _normal_chunk((seed, 7, b, c0), n, device)
+                x = _latent_chunk(seed, b, c0, min(chunk, L - c0), device, pattern)
                 amax = max(amax, float(x.abs().max()))
         scale = np.float32(amax) / np.float32(FP8_MAX)
     scale = np.float32(scale)
@@ -110,7 +119,7 @@ def _latent_codes(seed, lens_padded, device, scale=None):
         out = torch.empty((L, D_QK), dtype=torch.uint8, device=device)
         for c0 in range(0, L, chunk):
             m = min(chunk, L - c0)
-            x = _normal_chunk((seed, 7, b, c0), m * D_QK, device)
+            x = _latent_chunk(seed, b, c0, m, device, pattern).reshape(-1)
             y = torch.clamp(x / st, -FP8_MAX, FP8_MAX).to(torch.float8_e4m3fn)
             out[c0:c0 + m] = y.view(torch.uint8).view(m, D_QK)
         blocks.append(out)
@@ -142,9 +151,11 @@ def paginate(blocks, seed, device, *, permute=True, max_pages=None, extra_pages=
     return kv, torch.from_numpy(bt).to(device)
 
 
-def make_q(seed, B, T, H, device="cpu"):
+def make_q(seed, B, T, H, device="cpu", pattern=None):
     rng = np.random.default_rng([int(seed), 3])
     q = torch.from_numpy(rng.standard_normal((B, T, H, D_QK), dtype=np.float32))
+    if pattern is not None:
+        q = pattern.queries(q)
     return q.to(torch.bfloat16).to(device)
 
 
@@ -156,18 +167,164 @@ def make_latent(seed, B, T, device="cpu", amplitude=1.0):
 
 
 def make_decode_case(seed, lens, H, T=1, *, device="cpu", permute=True, max_pages=None,
-                     extra_pages=0, kv_scale=None, sm_scale=SM_SCALE) -> DecodeCase:
-    """Seeded decode inputs for contexts ``lens`` (each includes the T new positions)."""
+                     extra_pages=0, kv_scale=None, sm_scale=SM_SCALE, pattern=None) -> DecodeCase:
+    """Seeded decode inputs for contexts ``lens`` (each includes the T new positions).
+    ``pattern``: an optional stress pattern (below) that reshapes the latents and
+    queries before quantisation."""
     device = torch.device(device)
     lens = [int(x) for x in lens]
     padded = [((L + PAGE - 1) // PAGE) * PAGE for L in lens]
-    blocks, scale = _latent_codes(seed, padded, device, kv_scale)
+    if pattern is not None and kv_scale is None:
+        kv_scale = pattern.fixed_scale()
+    blocks, scale = _latent_codes(seed, padded, device, kv_scale, pattern)
     kv, bt = paginate(blocks, seed, device, permute=permute, max_pages=max_pages,
                       extra_pages=extra_pages)
-    q = make_q(seed, len(lens), T, H, device)
+    q = make_q(seed, len(lens), T, H, device, pattern)
     sl = torch.tensor(lens, dtype=torch.int32, device=device)
     ks = torch.tensor([scale], dtype=torch.float32, device=device)
     return DecodeCase(q, kv, ks, bt, sl, sm_scale, lens)
+
+
+# ----------------------------------------------------------------------------
+# Stress patterns: structured latents and queries that drive the softmax into
+# its hard regimes (peaked, climbing, long flat tails far below a peak) while
+# the values (latent dims [0, 512)) keep magnitudes where a bf16 answer can
+# meet the absolute tolerance.  Structure is planted along one direction u
+# spread evenly over the 64 positional dims [512, 576): a position's score
+# then moves with its planted amplitude times the query's alignment with u.
+# Input generation only: no attention arithmetic happens here.
+# ----------------------------------------------------------------------------
+
+def planted_direction(device="cpu"):
+    """Unit vector with 1/8 in each of the 64 positional dims, 0 elsewhere."""
+    u = torch.zeros(D_QK, dtype=torch.float32, device=device)
+    u[D_V:] = 0.125
+    return u
+
+
+class StressPattern:
+    """Base: N(0,1) latents and queries, unchanged."""
+
+    def latents(self, b, c0, x):  # x: fp32 [m, 576] of positions c0 ..
+        return x
+
+    def queries(self, q):  # q: fp32 [B, T, H, 576]
+        return q
+
+    def fixed_scale(self):  # None: scale = amax / 448
+        return None
+
+
+class PeakedQueries(StressPattern):
+    """Queries multiplied by ``gain``: scores gain times wider, a peaked softmax."""
+
+    def __init__(self, gain):
+        self.gain = float(gain)
+
+    def queries(self, q):
+        return q * self.gain
+
+
+class ClimbingKeys(StressPattern):
+    """Scores that climb: position p carries amplitude amp * ((p % period) + 1) / period
+    along u, and the queries of heads h % 2 == 0 align with u with weight ``align``
+    (the others keep N(0,1) queries, so both regimes share a call).  With a period
+    equal to a partition's positions every partition's largest score sits on its
+    last page and the running maximum moves again and again."""
+
+    def __init__(self, amp, period, align=8.0, q_noise=1.0):
+        self.amp, self.period, self.align, self.q_noise = float(amp), int(period), float(align), float(q_noise)
+
+    def latents(self, b, c0, x):
+        m = x.shape[0]
+        p = torch.arange(c0, c0 + m, device=x.device, dtype=torch.float32)
+        a = self.amp * (torch.remainder(p, self.period) + 1.0) / self.period
+        return x + a[:, None] * planted_direction(x.device)[None, :]
+
+    def queries(self, q):
+        q = q * self.q_noise
+        q[:, :, 0::2, :] += self.align * planted_direction()
+        return q
+
+
+class FirstPeak(StressPattern):
+    """One dominant position: position 0 of every request carries amplitude ``amp``
+    along u and every query is mostly u (noise ``q_noise``), so position 0 scores
+    ``gap`` natural-log units or more above all others."""
+
+    def __init__(self, amp, align=8.0, q_noise=0.05):
+        self.amp, self.align, self.q_noise = float(amp), float(align), float(q_noise)
+
+    def latents(self, b, c0, x):
+        if c0 == 0:
+            x = x.clone()
+            x[0] += self.amp * planted_direction(x.device)
+        return x
+
+    def queries(self, q):
+        return q * self.q_noise + self.align * planted_direction()
+
+
+class CoherentTail(StressPattern):
+    """The flush regime at its worst: position 0 of request b carries amplitude
+    ``amps[b]`` along u; every other position holds the same latent (a fixed
+    value vector with entries +-value, zero positional dims), so all of them
+    score exactly the same, some distance below position 0, and their rounding
+    errors add up coherently.  Queries are exactly ``align`` * u (zero value
+    dims), so that distance is align * amps[b] * sm_scale (natural log units)."""
+
+    def __init__(self, amps, align=8.0, value=1.0):
+        self.amps, self.align, self.value = [float(a) for a in amps], float(align), float(value)
+
+    def latents(self, b, c0, x):
+        sign = torch.where(torch.arange(D_V, device=x.device) % 3 == 0, -1.0, 1.0)
+        y = torch.zeros_like(x)
+        y[:, :D_V] = self.value * sign[None, :]
+        if c0 == 0:  # position 0: random values, positional dims exactly amp * u
+            y[0, :D_V] = x[0, :D_V]
+            y[0, D_V:] = self.amps[b % len(self.amps)] * planted_direction(x.device)[D_V:]
+        return y
+
+    def queries(self, q):
+        return torch.zeros_like(q) + self.align * planted_direction()
+
+
+class OutlierQueries(StressPattern):
+    """One channel of every query row (a different one per row) ``ratio`` times the
+    others' scale: the row is outlier * e_d + (outlier / ratio) * N(0,1), so the
+    exact two-term query split must carry elements 2^-10 of the row's maximum
+    (and below) while the scores stay of the usual size (outlier * x_d *
+    sm_scale)."""
+
+    def __init__(self, ratio=1024.0, outlier=16.0):
+        self.ratio, self.outlier = float(ratio), float(outlier)
+
+    def queries(self, q):
+        B, T, H, D = q.shape
+        q = q * (self.outlier / self.ratio)
+        idx = (torch.arange(B * T * H) * 37) % D
+        flat = q.view(-1, D)
+        rows = torch.arange(B * T * H)
+        flat[rows, idx] = torch.where(flat[rows, idx] >= 0, self.outlier, -self.outlier)
+        return q
+
+
+class ScaledCache(StressPattern):
+    """Latents times ``latent_gain`` quantised with a fixed ``kv_scale`` (not
+    amax / 448), and queries times ``q_gain``: a tiny scale with huge queries, or
+    a large scale with codes in e4m3's subnormal range."""
+
+    def __init__(self, latent_gain, kv_scale, q_gain):
+        self.latent_gain, self.kv_scale, self.q_gain = float(latent_gain), float(kv_scale), float(q_gain)
+
+    def latents(self, b, c0, x):
+        return x * self.latent_gain
+
+    def queries(self, q):
+        return q * self.q_gain
+
+    def fixed_scale(self):
+        return self.kv_scale
 
 
 @dataclass
