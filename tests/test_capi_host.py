@@ -272,10 +272,10 @@ def test_plan_splits_ragged_batches(L):
     counts of a sweep on GB300 (shards: 38.4 us at 7 against 40.6 at 6, 44.1
     at 8 and 50.2 at the automatic 4; whole workload: 168 us at 16 against 180
     at the automatic 14 and 212 at 18)."""
-    import bench
+    from mla_latent_kv_fp8_gb300.dcp import shard_plan
     lens = synth.verify_lens(4)
     Lb = L
-    plan = bench.dcp_verify_plan(lens, torch.zeros((16, 2048), dtype=torch.int32), 8, 4)
+    plan = shard_plan(lens, torch.zeros((16, 2048), dtype=torch.int32), 8, 4)
     for (table, sl), (T, H) in ((plan[0], (1, 48)), (plan[-1], (4, 12))):
         assert Lb.mla_plan_splits(16, T, H, sl.tolist(), table.shape[1], 152) == 7
     mp = -(-max(lens) // 64)
