@@ -1,5 +1,5 @@
-"""Host-side logic of bench.py that needs no GPU: the shard plan of the DCP
-multi-token verify measurement."""
+"""Host-side logic of bench.py that needs no GPU: parity bookkeeping, flop
+counts, the tensor roofline and the gate on recorded ncu counters."""
 import numpy as np
 import pytest
 import torch
@@ -8,32 +8,11 @@ import bench
 from mla_latent_kv_fp8_gb300 import synth
 
 
-@pytest.mark.parametrize("n_sh", [2, 8])
-def test_dcp_verify_plan_covers_each_history_once(n_sh):
-    lens = synth.verify_lens(4)  # the verify workload's contexts
-    B, T = len(lens), 4
-    max_pages = -(-max(lens) // 64)
-    bt = torch.stack([torch.randperm(10 * max_pages)[:max_pages] for _ in range(B)]).to(torch.int32)
-    plan = bench.dcp_verify_plan(lens, bt, n_sh, T)
-    assert len(plan) == n_sh
-    for b, L in enumerate(lens):
-        pages, pos = [], 0
-        for s, (table, sl) in enumerate(plan):
-            n = int(sl[b])
-            if s < n_sh - 1:
-                assert n % 64 == 0  # shards start on page boundaries
-            np_ = -(-n // 64)
-            pages += table[b, :np_].tolist()
-            pos += n
-        assert pos == L  # the shards tile the history exactly
-        assert pages == bt[b, :-(-L // 64)].tolist()  # in order, each page once
-        assert int(plan[-1][1][b]) >= T  # the draft positions lie in the last shard
-
-
 def test_dcp_verify_plan_rejects_short_histories():
+    from mla_latent_kv_fp8_gb300.dcp import shard_plan
     bt = torch.arange(4, dtype=torch.int32).reshape(1, 4)
     with pytest.raises(ValueError):
-        bench.dcp_verify_plan([7 * 64 + 2], bt, 8, 4)
+        shard_plan([7 * 64 + 2], bt, 8, 4)
 
 
 def test_parity_of_applies_the_tolerances():
@@ -70,3 +49,33 @@ def test_tensor_roofline_fields():
     assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
     assert abs(r["achieved"] - 1000.0) < 1e-6
     assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-3
+
+
+def test_device_code_digest_ignores_comments_and_host_code(tmp_path, monkeypatch):
+    """The ncu traffic record stays valid across comment and host-side edits of a
+    kernel file and is invalidated by any change to its device code."""
+    root = tmp_path
+    (root / "k.cu").write_text("__global__ void k(int* p) {\n    p[0] = 1;  // store\n}\n"
+                               + bench.HOST_SIDE_MARKER + "\nint launch() { return 0; }\n")
+    monkeypatch.setattr(bench, "ROOT", str(root))
+    d0 = bench.device_code_digest(["k.cu"])
+    (root / "k.cu").write_text("// a new header comment\n\n__global__ void k(int* p) {\n    p[0] = 1;  // the store\n}\n"
+                               + bench.HOST_SIDE_MARKER + "\nint launch() { return 1; }\n")
+    assert bench.device_code_digest(["k.cu"]) == d0
+    (root / "k.cu").write_text("__global__ void k(int* p) {\n    p[0] = 2;\n}\n" + bench.HOST_SIDE_MARKER + "\n")
+    assert bench.device_code_digest(["k.cu"]) != d0
+
+
+def test_ncu_traffic_record_is_gated_on_the_device_code():
+    import json
+    import os
+    p = os.path.join(bench.ROOT, "profiles", "ncu_traffic.json")
+    with open(p) as f:
+        d = json.load(f)
+    for key, e in d.items():
+        fam, workload = key.split("/")
+        r = bench.ncu_traffic(fam, workload)
+        current = e.get("device_code_digest") == bench.device_code_digest(bench.KERNEL_SOURCES[fam])
+        assert (r is not None) == current, key
+        if r is not None:
+            assert r["dram_bytes_per_launch"] == e["dram_bytes_per_launch"]
