@@ -52,6 +52,9 @@ struct DecodeParams {
     // rows each (the last CTA may have fewer)
     int row_ctas;
     int rows_per_cta;
+    // tcgen05 kernels: a moved reference maximum sits this far (log2 units)
+    // below the page maximum (set per launch from the partition length)
+    float ref_shift;
 };
 
 struct MergeParams {

@@ -24,17 +24,20 @@
 //     the latent, D[128 dims x 32] = V^T[128 x 64 pos] . [p1 | p2]^T, with V^T read
 //     from the same page tile as an MN-major operand (M=128, N=32).
 //   * Probabilities are taken against a per-head reference r that moves only
-//     when a score would exceed r + 8 (log2 units): P = 2^(s - r) in (0, 256],
+//     when a score would exceed r + 8.8 (log2 units): P = 2^(s - r) in (0, 445],
 //     stored as two e4m3 terms p1 + p2 / 16 (relative error ~2^-8, the bf16
 //     level).  Each lane first compares its own scores with r; one named
 //     barrier ORs that test over the warpgroup, and only when it is set do the
-//     warps reduce the page maxima and move r (new r = page max - 7), rescaling
+//     warps reduce the page maxima and move r (new r = page max - S), rescaling
 //     the accumulated output in TMEM in place.  Most pages skip the reductions.
-//     The new reference sits 7 units down so that the largest probability of
-//     the row starts at 2^7: far below it, e4m3's subnormal floor caps the
-//     absolute error of each p1 + p2/16 at ~2^-14, i.e. 2^-21 of the largest
-//     weight, and ten thousand equal positions there lose at most ~0.5% of
-//     their weight together (at 4 units down they lost up to ~4%).
+//     The shift S (4..7, p.ref_shift) bounds what e4m3's subnormal floor can
+//     take: each p1 + p2/16 is off by at most ~2^-14 in absolute terms, i.e.
+//     2^-(14+S) of the row's largest weight, so the n positions a warpgroup
+//     accumulates lose at most n * 2^-(14+S) of it together; the host picks
+//     S = log2(n) - 6 within [4, 7] (at most 2^-8 lost), since every further
+//     unit of S makes references move more often.  The rescale of a move waits
+//     for the previous PV, so it runs after the page's probabilities are
+//     written, overlapping that wait.
 //   * Warp roles: warp 0 TMA producer; three MMA-issuing warps (warp 1: QK^T of
 //     even pages, warp 3: QK^T of odd pages, warp 2: PV of every page), because
 //     one thread can issue a tcgen05.mma only every ~50 cycles; and two
@@ -53,6 +56,7 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
+#include <cmath>
 #include <mutex>
 
 #include "mla_internal.cuh"
@@ -78,8 +82,8 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSCol0 = 0;               // S buffers: 4 x 32 cols at [0, 128)
 constexpr uint32_t kSCols = 32;
 constexpr uint32_t kOCol0 = 128;             // O buffers: one per warpgroup, 128 cols each
-constexpr float kHeadroom = 8.f;             // log2 units a score may exceed its head's reference
-constexpr float kShift = 7.f;                // a new reference sits this far below the page max
+// log2 units a score may exceed its head's reference: P = 2^(s - r) <= 2^8.8 < 448
+constexpr float kHeadroom = 8.8f;
 static_assert(kOCol0 + 128 * kGroups <= kTmemCols, "TMEM budget");
 
 
@@ -466,6 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool fail = false;
         int k = 0;
         int32_t pid_next = g < n_pages ? __ldg(bt + g) : 0;
+        const float ref_shift = p.ref_shift;
         for (int i = g; i < n_pages; i += kGroups, ++k) {
             const int sb = i % kSBufs;           // score buffer
             const int kb = k & 1;                // this group's probability / statistics buffer
@@ -475,6 +480,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int pos = (pg_begin + i) * kPage + pr;
             float s[kHL];
             bool over = false;  // a score of this lane exceeds its head's reference + headroom
+            bool rescale = false;  // a reference moved after this group's first page
+            float a_mv = 1.f;      // lane h < 16: factor for head h's accumulated columns
             // ---- scores of this page ----
             if (!fail) fail = !warp_wait(&S.s_full[sb], (i / kSBufs) & 1, abort, p.err);
             if (!fail) {
@@ -528,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const bool need = lane < kRows && t > r_l + kHeadroom;
                 if (__ballot_sync(0xffffffffu, need)) {
-                    const float rn = need ? t - kShift : r_l;
+                    const float rn = need ? t - ref_shift : r_l;
                     const float a = need ? exp2f(r_l - rn) : 1.f;  // r_l = -inf: nothing to keep
                     r_l = rn;
                     if (p.test_counts && quad == 0 && lane == 0) {
@@ -540,28 +547,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         rr[j] = __shfl_sync(0xffffffffu, rn, kHL * half + j);
                         lp[j] *= __shfl_sync(0xffffffffu, a, kHL * half + j);
                     }
-
-                    if (k > 0) {
-                        // The tile holds PV of this group's pages 0..k-1: wait for the
-                        // last of them, then scale every head's columns.
-                        if (!warp_wait(&S.pv_done[g][(k - 1) & 1], ((k - 1) >> 1) & 1, abort, p.err)) {
-                            fail = true;
-                        } else {
-                            tc_fence_after();
-#pragma unroll
-                            for (int c = 0; c < 4; ++c) {
-                                uint32_t v[32];
-                                tmem_ld32(to + 32 * c, v);
-                                tmem_wait_ld();
-#pragma unroll
-                                for (int j = 0; j < 32; ++j) {
-                                    const float al = __shfl_sync(0xffffffffu, a, j & 15);  // lane h: head h
-                                    if ((j & 15) < kRows) v[j] = __float_as_uint(__uint_as_float(v[j]) * al);
-                                }
-                                tmem_st32(to + 32 * c, v);
-                            }
-                            tmem_wait_st();
-                        }
+                    if (k > 0) {  // the accumulated tile is rescaled below
+                        rescale = true;
+                        a_mv = a;
                     }
                 }
             }
@@ -599,10 +587,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                fence_async_smem();
-                tc_fence_before();  // TMEM stores of a rescale precede the next PV
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&S.p_full[g][kb]);
+                if (rescale) {
+                    // The tile holds PV of this group's pages 0..k-1: wait for the
+                    // last of them (the probabilities above overlapped that wait),
+                    // then scale every head's columns.
+                    if (!warp_wait(&S.pv_done[g][(k - 1) & 1], ((k - 1) >> 1) & 1, abort, p.err)) {
+                        fail = true;
+                    } else {
+                        tc_fence_after();
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            uint32_t v[32];
+                            tmem_ld32(to + 32 * c, v);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                const float al = __shfl_sync(0xffffffffu, a_mv, j & 15);  // lane h: head h
+                                if ((j & 15) < kRows) v[j] = __float_as_uint(__uint_as_float(v[j]) * al);
+                            }
+                            tmem_st32(to + 32 * c, v);
+                        }
+                        tmem_wait_st();
+                    }
+                }
+                if (!fail) {
+                    fence_async_smem();
+                    tc_fence_before();  // TMEM stores of a rescale precede the next PV
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&S.p_full[g][kb]);
+                }
             }
         }
 
@@ -783,6 +796,14 @@ cudaError_t encode_cache_maps(CUtensorMap* map3, CUtensorMap* map2, const uint8_
 cudaError_t launch_tc_wide(const DecodeParams& p, const CUtensorMap& map, const CUtensorMap& map_box,
                            cudaStream_t stream);
 
+// The smallest shift S in [4, 7] with positions <= 2^(S + 6): the n positions
+// one warpgroup accumulates then lose at most n * 2^-(14 + S) <= 2^-8 of the
+// row's largest weight to e4m3's subnormal floor.
+float reference_shift(long long positions) {
+    const double s = std::log2(static_cast<double>(positions > 1 ? positions : 1)) - 6.0;
+    return static_cast<float>(s < 4.0 ? 4.0 : (s > 7.0 ? 7.0 : s));
+}
+
 bool tc_supports(const DecodeParams& p, int cc_major, int cc_minor) {
     return cc_major == 10 && cc_minor == 3 && p.H * p.T <= kMaxRowsTc && p.num_pages >= 1 &&
            p.num_pages * kPage < (1ll << 31);
@@ -829,6 +850,9 @@ cudaError_t launch_tc_decode(const DecodeParams& p, cudaStream_t stream, bool* h
     }
     const int HT = p.H * p.T;
     DecodeParams q = p;
+    // A warpgroup of the 12-head kernel accumulates every other page of a
+    // partition; one of the wide kernel every page (for its rows).
+    q.ref_shift = reference_shift(64ll * (HT > kNq ? p.chunk_pages : (p.chunk_pages + 1) / 2));
     if (HT > kNq) {
         // More than 16 rows: the wide kernel, ceil(H*T / 32) CTAs per
         // (partition, request) with the rows shared evenly.

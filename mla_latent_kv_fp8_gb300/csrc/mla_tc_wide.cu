@@ -25,9 +25,10 @@
 //     needed at the end.  Each lane works on 4 rows of one position.
 //   * PV: D[128 dims x 64] += V^T[128 x 64 pos] . [p1 | p2]^T per 128-dim block,
 //     P = p1 + p2 / 16 in e4m3 (relative error ~2^-8), 8 MMAs of N = 64 per page.
-//     A row's reference moves when a score would exceed it by 8 (log2 units)
-//     and then sits 7 below the page max, so the largest probability starts at
-//     2^7 and the e4m3 floor of tiny probabilities lies ~2^-21 below it.
+//     A row's reference moves when a score would exceed it by 8.8 (log2
+//     units) and then sits S = p.ref_shift (4..7, from the partition length)
+//     below the page max, so the largest probability starts at 2^S and the
+//     e4m3 floor of tiny probabilities lies ~2^-(14+S) below it.
 //   * TMEM: 2 score tiles x 128 columns + output 4 blocks x 64 columns = 512.
 // Warp roles (640 threads, one CTA per SM): warp 0 TMA producer (ring of 4
 // pages), warps 1 and 3 issue QK^T, warp 2 issues PV, warps 4-19 are the four
@@ -66,8 +67,8 @@ constexpr uint32_t kWTmemCols = 512;
 constexpr uint32_t kWSCols = 2 * kWN;        // 128: one score tile (K-half a | K-half b)
 constexpr uint32_t kWOCol0 = kWSBufs * kWSCols;  // 256: output tile, block c at + 64 c
 constexpr int kWSetupBar = 1 + kWGroups;     // named barrier of the set-up (warps 1..19)
-constexpr float kWHeadroom = 8.f;            // log2 units a score may exceed its row's reference
-constexpr float kWShift = 7.f;               // a new reference sits this far below the page max
+// log2 units a score may exceed its row's reference: P = 2^(s - r) <= 2^8.8 < 448
+constexpr float kWHeadroom = 8.8f;
 static_assert(kWOCol0 + 4 * kWN <= kWTmemCols, "TMEM budget");
 // The probabilities of page i go to buffer i % kWPBufs, last read by the PV of
 // page i - kWPBufs.  With as many buffers as ring slots that PV has finished
@@ -475,6 +476,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
         }
         bool fail = false;
         int32_t pid_next = __ldg(bt);
+        const float ref_shift = p.ref_shift;
         for (int i = 0; i < n_pages; ++i) {
             const int sb = i % kWSBufs, kb = i % kWPBufs, par = i & 1;
             const int32_t pid = pid_next;
@@ -484,6 +486,8 @@ __global__ void __launch_bounds__(kWThreads, 1)
             const bool in_part = page_ok && pos < p_end;
             float s[kWRL];
             bool over = false;  // a score of this lane exceeds its row's reference + headroom
+            bool rescale = false;  // a reference moved after the partition's first page
+            float a_mv = 1.f;      // lane h < 8: factor for group row h's accumulated columns
 #pragma unroll
             for (int j = 0; j < kWRL; ++j) s[j] = NEG;
             // ---- scores of this page ----
@@ -539,7 +543,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
                 }
                 const bool need = lane < kWRg && t > r_l + kWHeadroom;
                 if (__ballot_sync(0xffffffffu, need)) {
-                    const float rn = need ? t - kWShift : r_l;
+                    const float rn = need ? t - ref_shift : r_l;
                     const float a = need ? exp2f(r_l - rn) : 1.f;  // r_l = -inf: nothing to keep
                     r_l = rn;
                     if (p.test_counts && quad == 0 && lane == 0) {
@@ -551,32 +555,9 @@ __global__ void __launch_bounds__(kWThreads, 1)
                         rr[j] = __shfl_sync(0xffffffffu, rn, kWRL * half + j);
                         lp[j] *= __shfl_sync(0xffffffffu, a, kWRL * half + j);
                     }
-                    if (i > 0) {
-                        // The tile holds PV of pages 0..i-1: wait for the last one, then
-                        // scale this group's p1 and p2 columns (every warp its lane quadrant).
-                        const int pk = (i - 1) % kWPBufs;
-                        if (!warp_wait(&S.pv_done[pk], ((i - 1) / kWPBufs) & 1, abort, p.err)) {
-                            fail = true;
-                        } else {
-                            tc_fence_after();
-                            float al[kWRg];
-#pragma unroll
-                            for (int j = 0; j < kWRg; ++j) al[j] = __shfl_sync(0xffffffffu, a, j);
-#pragma unroll
-                            for (int c = 0; c < 4; ++c) {
-#pragma unroll
-                                for (int t2 = 0; t2 < 2; ++t2) {
-                                    const uint32_t col = to + kWN * c + kWRows * t2;
-                                    uint32_t v[8];
-                                    tmem_ld8(col, v);
-                                    tmem_wait_ld();
-#pragma unroll
-                                    for (int j = 0; j < kWRg; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * al[j]);
-                                    tmem_st8(col, v);
-                                }
-                            }
-                            tmem_wait_st();
-                        }
+                    if (i > 0) {  // the accumulated columns are rescaled below
+                        rescale = true;
+                        a_mv = a;
                     }
                 }
             }
@@ -608,10 +589,40 @@ __global__ void __launch_bounds__(kWThreads, 1)
                         q4[0] = q4[1] = q4[2] = q4[3] = make_uint4(0, 0, 0, 0);
                     }
                 }
-                fence_async_smem();
-                tc_fence_before();  // TMEM stores of a rescale precede the next PV
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&S.p_full[kb]);
+                if (rescale) {
+                    // The tile holds PV of pages 0..i-1: wait for the last one (the
+                    // probabilities above overlapped that wait), then scale this
+                    // group's p1 and p2 columns (every warp its lane quadrant).
+                    const int pk = (i - 1) % kWPBufs;
+                    if (!warp_wait(&S.pv_done[pk], ((i - 1) / kWPBufs) & 1, abort, p.err)) {
+                        fail = true;
+                    } else {
+                        tc_fence_after();
+                        float al[kWRg];
+#pragma unroll
+                        for (int j = 0; j < kWRg; ++j) al[j] = __shfl_sync(0xffffffffu, a_mv, j);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                uint32_t v[8];
+                                tmem_ld8(to + kWN * c + kWRows * u, v);
+                                tmem_wait_ld();
+#pragma unroll
+                                for (int j = 0; j < kWRg; ++j)
+                                    v[j] = __float_as_uint(__uint_as_float(v[j]) * al[j]);
+                                tmem_st8(to + kWN * c + kWRows * u, v);
+                            }
+                        }
+                        tmem_wait_st();
+                    }
+                }
+                if (!fail) {
+                    fence_async_smem();
+                    tc_fence_before();  // TMEM stores of a rescale precede the next PV
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&S.p_full[kb]);
+                }
             }
         }
 
