@@ -171,6 +171,15 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 }  // namespace
 
+void internal_carve_scratch(DecodeParams& p, void* ws) {
+    const size_t out_bytes = (size_t)p.n_splits * p.B * p.T * p.H * kDv * sizeof(float);
+    const size_t lse_bytes = (size_t)p.n_splits * p.B * p.T * p.H * sizeof(float);
+    char* base = static_cast<char*>(ws);
+    p.part_out = reinterpret_cast<float*>(base);
+    p.part_lse = reinterpret_cast<float*>(base + ((out_bytes + 255) & ~size_t(255)));
+    p.lpt_order = reinterpret_cast<int2*>(base + ((out_bytes + 255) & ~size_t(255)) + ((lse_bytes + 255) & ~size_t(255)));
+}
+
 // Accessors for the library's other host translation units (mla_host.h).
 mla_status_t internal_fail(mla_status_t st, const char* msg) { return fail(st, "%s", msg); }
 mla_status_t internal_cuda_fail(cudaError_t e, const char* what) { return cuda_fail(e, what); }
@@ -457,7 +466,8 @@ size_t mla_decode_workspace_bytes(int32_t B, int32_t T, int32_t H, int32_t n_spl
     const size_t rows = (size_t)B * T * H;
     const size_t out_bytes = (size_t)n_splits * rows * kDv * sizeof(float);
     const size_t lse_bytes = (size_t)n_splits * rows * sizeof(float);
-    return ((out_bytes + 255) & ~size_t(255)) + lse_bytes;
+    const size_t order_bytes = (size_t)n_splits * B * 2 * sizeof(int32_t);  // longest-first unit order
+    return ((out_bytes + 255) & ~size_t(255)) + ((lse_bytes + 255) & ~size_t(255)) + order_bytes;
 }
 
 mla_status_t mla_device_error(int32_t* code, void* stream) {
@@ -495,9 +505,7 @@ mla_status_t mla_decode_paged(const mla_tensor_t* q, const mla_tensor_t* kv_cach
         void* ws = nullptr;
         const size_t need = mla_decode_workspace_bytes(p.B, p.T, p.H, p.n_splits);
         if ((st = get_scratch(need, s, &ws)) != MLA_OK) return st;
-        const size_t out_bytes = (size_t)p.n_splits * p.B * p.T * p.H * kDv * sizeof(float);
-        p.part_out = static_cast<float*>(ws);
-        p.part_lse = reinterpret_cast<float*>(static_cast<char*>(ws) + ((out_bytes + 255) & ~size_t(255)));
+        internal_carve_scratch(p, ws);
     }
     return internal_launch_decode(p, s);
 }

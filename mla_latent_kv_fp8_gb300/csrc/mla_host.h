@@ -34,6 +34,10 @@ mla_status_t internal_prepare_decode(const mla_tensor_t* q, const mla_tensor_t* 
                                      const mla_tensor_t* out, const mla_tensor_t* lse, DecodeParams* p,
                                      bool* empty);
 
+// Points p.part_out and p.part_lse (the fp32 partials of the split-KV kernel)
+// into split scratch of at least mla_decode_workspace_bytes(...) bytes.
+void internal_carve_scratch(DecodeParams& p, void* ws);
+
 // Launches a prepared decode on `stream`: the split-KV kernel of the family
 // mla_set_impl selected (with the calling thread's profile events and test
 // hooks), then, when p.n_splits > 1, the split combine over p.part_out /

@@ -55,6 +55,9 @@ struct DecodeParams {
     // tcgen05 kernels: a moved reference maximum sits this far (log2 units)
     // below the page maximum (set per launch from the partition length)
     float ref_shift;
+    // 12-head tcgen05 kernel, more units than SMs: the longest-first order of
+    // the units, {b * n_splits + split, seq_len} per launch index (split scratch)
+    int2* lpt_order;
 };
 
 struct MergeParams {

@@ -31,8 +31,8 @@ using namespace mergedev;
 // Launched as a programmatic dependent of the decode kernel (pdl): wait for
 // its partials, and let the next kernel's CTAs be scheduled meanwhile (the
 // decode kernel waits for this one before reading anything).
-__device__ __forceinline__ void wait_for_producer(int pdl) {
-    if (pdl) {
+__device__ __forceinline__ void wait_for_producer(const MergeParams& p) {
+    if (p.pdl) {
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         asm volatile("griddepcontrol.wait;" ::: "memory");
     }
@@ -40,7 +40,7 @@ __device__ __forceinline__ void wait_for_producer(int pdl) {
 
 template <bool kBf16In>
 __global__ void __launch_bounds__(256) merge_warp_kernel(MergeParams p) {
-    wait_for_producer(p.pdl);
+    wait_for_producer(p);
     const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (gw >= p.rows * 8) return;
     merge_warp<kBf16In>(p, gw >> 3, static_cast<int>(gw & 7), threadIdx.x & 31);
@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(256) merge_warp_kernel(MergeParams p) {
 
 template <bool kBf16In>
 __global__ void __launch_bounds__(256, kBf16In ? 3 : 2) merge_row_kernel(MergeParams p) {
-    wait_for_producer(p.pdl);
+    wait_for_producer(p);
     const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (row >= p.rows) return;
     merge_row<kBf16In>(p, row, threadIdx.x & 31);
@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(256, kBf16In ? 3 : 2) merge_row_kernel(MergePa
 
 template <bool kBf16In>
 __global__ void __launch_bounds__(256) merge_cta_kernel(MergeParams p) {
-    wait_for_producer(p.pdl);
+    wait_for_producer(p);
     __shared__ CtaScratch sh;
     merge_cta<kBf16In>(p, blockIdx.x >> 4, static_cast<int>(blockIdx.x & 15), threadIdx.x, sh,
                        [] { __syncthreads(); });

@@ -85,10 +85,6 @@ extern "C" mla_status_t mla_decode_paged_noalloc(const mla_tensor_t* q, const ml
                  need, kNoAllocScratchBytes);
         return internal_fail(MLA_ERR_UNSUPPORTED, msg);
     }
-    if (p.n_splits > 1) {
-        const size_t out_bytes = (size_t)p.n_splits * p.B * p.T * p.H * kDv * sizeof(float);
-        p.part_out = static_cast<float*>(scratch);
-        p.part_lse = reinterpret_cast<float*>(static_cast<char*>(scratch) + ((out_bytes + 255) & ~size_t(255)));
-    }
+    if (p.n_splits > 1) internal_carve_scratch(p, scratch);
     return internal_launch_decode(p, static_cast<cudaStream_t>(stream));
 }

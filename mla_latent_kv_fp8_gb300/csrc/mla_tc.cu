@@ -46,8 +46,9 @@
 //     the probabilities and hands them to the PV issuer; PV accumulates into
 //     that warpgroup's own output tile in TMEM (lane = latent dim) over all of
 //     its pages.  Each thread keeps fp32 partial normalisers of its positions.
-//   * At the end the warpgroup without the last page parks its tile in a free
-//     page slot; the other combines it with its own and stores the rows.
+//   * At the end the warpgroup without the last page hands over its references
+//     and normalisers; the other reads both tiles from TMEM, combines them and
+//     stores the rows.
 //   * Every wait is bounded; on timeout the kernel records an error, drains its
 //     own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -82,6 +83,8 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSCol0 = 0;               // S buffers: 4 x 32 cols at [0, 128)
 constexpr uint32_t kSCols = 32;
 constexpr uint32_t kOCol0 = 128;             // O buffers: one per warpgroup, 128 cols each
+constexpr int kLptMaxB = 1024;               // longest-first launches order at most this many requests
+constexpr int kLptThreads = 1024;            // the ordering kernel: one thread per request
 // log2 units a score may exceed its head's reference: P = 2^(s - r) <= 2^8.8 < 448
 constexpr float kHeadroom = 8.8f;
 static_assert(kOCol0 + 128 * kGroups <= kTmemCols, "TMEM budget");
@@ -93,7 +96,8 @@ struct Smem {
     uint8_t pp[kGroups][2][kPpBytes];        // [p1 | p2] MN-major, no swizzle, per group page
     float red_m[kGroups][2][kNq][4];         // [group][iter parity][head][warp] tile maxima
     float red_l[kGroups][kNq][4];            // per group: end-of-loop normaliser partials
-    float fin[2][kNq];                       // parked warpgroup: final reference / normaliser by head
+    float fin[2][kNq];                       // other warpgroup: final reference / normaliser by head
+    int fin_bad;                             // the other warpgroup's tile is incomplete (a wait gave up)
     alignas(16) float row_scale[kNq];        // kv_scale * sm_scale * log2(e) * 2^-e
     alignas(16) int rowlim[kNq];             // visible prefix per row; -1 = padding
     uint64_t full[kStages], empty[kStages];
@@ -134,25 +138,89 @@ __device__ __forceinline__ void split_p(float a0, float a1, uint32_t& c1, uint32
         __nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&r), __NV_SATFINITE, __NV_E4M3));
 }
 
-// kRows: rows (t, h) this instantiation keeps in registers (12 or 16); the MMA
-// operands always use 16-row blocks (rows >= H*T are zero).
+// Longest-first launches (more units than SMs): the order of all B * n_splits
+// (request, partition) units, computed once per call by one CTA from the
+// device-resident lengths, before the decode kernel (which waits for it).
+// Full-chunk units come first (request-major), then each request's partial
+// chunk, longest remainder first (ties: lower request first); the decode CTAs
+// are dispatched in launch order, so the SMs that free up take the longest
+// units left and end within about one short unit of each other.  Entry k is
+// {b * n_splits + split, seq_len of b}, or {-1, 0} past the last unit with
+// history.  The empty units (partitions past a request's end) get their empty
+// partial (lse = -inf) here; a length outside [0, 64 * max_pages], or in
+// (0, T), reads nothing and sets device error 3.
+__global__ void __launch_bounds__(kLptThreads, 1) lpt_order_kernel(const DecodeParams p) {
+    __shared__ int full_pfx[kLptMaxB + 1];
+    __shared__ int rem_s[kLptMaxB];
+    __shared__ int warp_sum[kLptThreads / 32];
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");  // they wait for this grid to finish
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int B = p.B, chunk = p.chunk_pages, n_splits = p.n_splits, HT = p.H * p.T;
+    int L = 0, full = 0, rem = 0;
+    if (tid < B) {
+        L = __ldg(p.seq_lens + tid);
+        if (L < 0 || L > p.max_pages * kPage || (L > 0 && L < p.T)) {
+            atomicCAS(p.err, 0, kErrSeqRange);
+            L = 0;
+        }
+        const int pages = (L + kPage - 1) / kPage;
+        full = pages / chunk;
+        rem = pages - full * chunk;
+        rem_s[tid] = rem;
+    }
+    // exclusive prefix over the requests of their full-chunk units
+    int x = full;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, d);
+        if (lane >= d) x += y;
+    }
+    if (lane == 31) warp_sum[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = warp_sum[lane];
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, w, d);
+            if (lane >= d) w += y;
+        }
+        warp_sum[lane] = w;  // inclusive prefix of the warps' sums
+    }
+    __syncthreads();
+    x += warp > 0 ? warp_sum[warp - 1] : 0;  // inclusive prefix of this request
+    if (tid < B) full_pfx[tid] = x - full;
+    if (tid == kLptThreads - 1) full_pfx[B] = x;  // every full unit (threads >= B add 0)
+    const int n_part = __syncthreads_count(tid < B && rem > 0);  // also publishes full_pfx and rem_s
+    const int n_full = full_pfx[B];
+    int2* order = p.lpt_order;
+    if (tid < B) {
+        for (int sp = 0; sp < full; ++sp) order[full_pfx[tid] + sp] = make_int2(tid * n_splits + sp, L);
+        if (rem > 0) {
+            int ahead = 0;  // partial chunks ordered before this one
+            for (int o = 0; o < B; ++o) {
+                const int r2 = rem_s[o];
+                ahead += (r2 > rem || (r2 == rem && o < tid)) ? 1 : 0;
+            }
+            order[n_full + ahead] = make_int2(tid * n_splits + full, L);
+        }
+        for (int sp = full + (rem > 0 ? 1 : 0); sp < n_splits; ++sp)
+            for (int r = 0; r < HT; ++r) p.part_lse[((int64_t)sp * B + tid) * HT + r] = -INFINITY;
+    }
+    for (int k = n_full + n_part + tid; k < B * n_splits; k += kLptThreads) order[k] = make_int2(-1, 0);
+}
+
+// One (request b, partition split) unit, start to finish: barriers, TMEM,
+// query operand, the warp roles, the epilogue, and a last barrier after which
+// every copy and MMA has drained.  Returns false (having written an empty
+// partial and allocated nothing) when the unit holds no history.
 template <int kRows>
-__global__ void __launch_bounds__(kThreads, 1)
-    tc_decode_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_box,
-                     const DecodeParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+__device__ __forceinline__ bool decode_unit(const CUtensorMap* tmap, const CUtensorMap* tmap_box,
+                                            const DecodeParams& p, Smem& S, int b, int split, int L_known) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int HT = p.H * p.T;
-    // Launched as a programmatic dependent of the previous kernel on the stream:
-    // everything before this point overlaps its tail; nothing is read before it.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    // One CTA per (partition, request) with all of its H*T <= 16 rows (units
-    // of more rows run on the wide kernel).
-    const int split = blockIdx.x, b = blockIdx.y;
-    const int HTc = HT;                          // rows of this CTA
+    const int HTc = HT;                          // rows of every unit (all of the request's)
     volatile int* abort = &S.abort;
-
     // Global loads that depend only on the launch indices go out together,
     // before any of their values is needed: the producer's first 64 page ids
     // (one per lane, in two windows of 32) and the query rows of warps 1..11.
@@ -162,8 +230,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint4 qv[2][3];  // rows warp - 1 and warp + 10, 16-byte chunks lane + 32k
     if (warp == 0) {
         if (lane == 0) {
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_box)) : "memory");
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap_box)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
         }
         pid_cur = pg_begin + lane < p.max_pages ? __ldg(bt_cta + lane) : 0;
         pid_nxt = pg_begin + 32 + lane < p.max_pages ? __ldg(bt_cta + 32 + lane) : 0;
@@ -179,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     }
-    int L = __ldg(p.seq_lens + b);
+    int L = L_known >= 0 ? L_known : __ldg(p.seq_lens + b);
     const float kv_scale = __ldg(p.kv_scale);
     if (L < 0 || L > p.max_pages * kPage || (L > 0 && L < p.T)) {
         if (tid == 0) atomicCAS(p.err, 0, kErrSeqRange);
@@ -201,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int idx = tid; idx < HTc; idx += kThreads)
                 p.part_lse[(int64_t)split * p.B * HT + row0 + idx] = -INFINITY;
         }
-        return;
+        return false;
     }
 
     // ---------------- set-up: barriers, TMEM, query operand ----------------
@@ -223,6 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 3; ++i) mbar_init(&S.mma_done[i], 1);
         S.abort = 0;
+        S.fin_bad = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -244,9 +313,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t dst = smem_u32(S.slot[s]);
         if (i < kStages) {
 #pragma unroll
-            for (int j = 0; j < kBoxes; ++j) tma_load_box(dst + j * kBoxBytes, &tmap_box, 64 * j, pid * kPage, &S.full[s]);
+            for (int j = 0; j < kBoxes; ++j) tma_load_box(dst + j * kBoxBytes, tmap_box, 64 * j, pid * kPage, &S.full[s]);
         } else {
-            tma_load_page(dst, &tmap, pid * kPage, &S.full[s]);
+            tma_load_page(dst, tmap, pid * kPage, &S.full[s]);
         }
     };
     if (warp == 0 && n_pages > 0 && !p.test_stall_copies) {
@@ -265,6 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+
     // Query rows: warps 1..11 prepare rows warp - 1 and warp + 10 (< 16).
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
@@ -619,24 +689,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
 
-        // ---- the group's accumulated tile: O = D(p1) + D(p2) / 16 ----
+        // ---- the group's accumulated tile is complete once its last PV is ----
         const int cnt = n_pages > g ? (n_pages - g + kGroups - 1) / kGroups : 0;
         bool o_ok = !fail && cnt > 0;
         if (o_ok) o_ok = warp_wait(&S.pv_done[g][(cnt - 1) & 1], ((cnt - 1) >> 1) & 1, abort, p.err);
-        float o[4][kRows];
-        if (o_ok) tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            uint32_t v[32];
-            if (o_ok) {
-                tmem_ld32(to + 32 * c, v);
-                tmem_wait_ld();
-            }
-#pragma unroll
-            for (int h = 0; h < kRows; ++h)
-                o[c][h] = o_ok ? fmaf(__uint_as_float(v[16 + h]), 0.0625f, __uint_as_float(v[h])) : 0.f;
-        }
-        float m_run = r_l;
+        const float m_run = r_l;
 
         // ---- this group's normaliser: reduce the per-thread partials ----
         {
@@ -655,30 +712,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             l_run = (vl.x + vl.y) + (vl.z + vl.w);
         }
 
-        // ---- combine the warpgroups' running states; write the answer ----
+        // ---- combine the warpgroups' states; write the answer ----
         // The warpgroup that owns the partition's last page finishes last.  The
-        // other one parks its tile as [row][512] fp32, with its references and
-        // normalisers, in the slot of its own last page (or in a slot no page
-        // used) and leaves; the last one combines that tile with its own
-        // registers and stores the answer rows straight to global memory.
-        static_assert(kGroups == 2, "the parking slot assumes two warpgroups");
+        // other one publishes its references and normalisers and leaves its
+        // tile in TMEM; the last one reads both tiles (its warps see the same
+        // TMEM lanes in both) 32 columns at a time and stores the answer rows
+        // straight to global memory.
+        static_assert(kGroups == 2, "the hand-over assumes two warpgroups");
         const int gc = (n_pages - 1) % kGroups;  // combining warpgroup (n_pages >= 1 here)
-        const int gp = 1 - gc;                   // parking warpgroup
+        const int gp = 1 - gc;                   // the other one
         const int cnt_p = n_pages > gp ? (n_pages - gp + kGroups - 1) / kGroups : 0;
-        float* tile = reinterpret_cast<float*>(S.slot[cnt_p > 0 ? (gp + kGroups * (cnt_p - 1)) % kStages : kStages - 1]);
         if (g == gp) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-                for (int h = 0; h < kRows; ++h) tile[h * kDv + 128 * c + d] = o[c][h];
             if (quad == 0 && lane < kNq) {
                 S.fin[0][lane] = m_run;
                 S.fin[1][lane] = l_run;
             }
+            if (!o_ok && cnt > 0 && lane == 0) S.fin_bad = 1;  // its tile is not to be read
+            tc_fence_before();
             __threadfence_block();
-            asm volatile("bar.arrive 4, 256;" ::: "memory");  // tile and state parked
+            asm volatile("bar.arrive 4, 256;" ::: "memory");  // state published, tile complete
         } else {
             asm volatile("bar.sync 4, 256;" ::: "memory");
+            tc_fence_after();
+            const bool other_ok = cnt_p > 0 && S.fin_bad == 0;
             const bool direct = p.n_splits == 1;
             // lane h: the weight of each tile (normaliser and kv_scale folded in)
             float w_own = 0.f, w_park = 0.f;
@@ -704,25 +760,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            // every load of the parked tile first, then every store
-#pragma unroll
-            for (int h = 0; h < kRows; ++h) {
-                const float wo = __shfl_sync(0xffffffffu, w_own, h);
-                const float wp = __shfl_sync(0xffffffffu, w_park, h);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) o[c][h] = fmaf(tile[h * kDv + 128 * c + d], wp, o[c][h] * wo);
-            }
             const int64_t row0 = (int64_t)b * HT;  // this CTA's first answer row
+            const uint32_t tp = tmem + (static_cast<uint32_t>(32 * quad) << 16) + kOCol0 + 128 * gp;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                // O = D(p1) + D(p2) / 16 of each tile, weighted
+                float v[kRows];
+                uint32_t t[32];
+                if (o_ok) {
+                    tmem_ld32(to + 32 * c, t);
+                    tmem_wait_ld();
+                }
 #pragma unroll
-            for (int h = 0; h < kRows; ++h) {
-                if (h < HTc) {
+                for (int h = 0; h < kRows; ++h) {
+                    const float wo = __shfl_sync(0xffffffffu, w_own, h);
+                    v[h] = o_ok ? fmaf(__uint_as_float(t[16 + h]), 0.0625f, __uint_as_float(t[h])) * wo : 0.f;
+                }
+                if (other_ok) {
+                    tmem_ld32(tp + 32 * c, t);
+                    tmem_wait_ld();
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
+                    for (int h = 0; h < kRows; ++h) {
+                        const float wp = __shfl_sync(0xffffffffu, w_park, h);
+                        v[h] = fmaf(fmaf(__uint_as_float(t[16 + h]), 0.0625f, __uint_as_float(t[h])), wp, v[h]);
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < kRows; ++h) {
+                    if (h < HTc) {
                         const int64_t at = (row0 + h) * kDv + 128 * c + d;
                         if (direct)
-                            p.out[at] = __bfloat16_as_ushort(__float2bfloat16_rn(o[c][h]));
+                            p.out[at] = __bfloat16_as_ushort(__float2bfloat16_rn(v[h]));
                         else
-                            p.part_out[(int64_t)split * p.B * HT * kDv + at] = o[c][h];
+                            p.part_out[(int64_t)split * p.B * HT * kDv + at] = v[h];
                     }
                 }
             }
@@ -732,8 +802,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) {
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+    return true;
+}
+
+template <int kRows, bool kLpt>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_decode_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_box,
+                     const __grid_constant__ DecodeParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5;
+    // Launched as a programmatic dependent of the previous kernel on the stream:
+    // everything before this point overlaps its tail; nothing is read before it.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    bool tmem_held;  // the unit had pages (its set-up allocated TMEM)
+    if constexpr (!kLpt) {
+        // one CTA per (partition, request) unit
+        tmem_held = decode_unit<kRows>(&tmap, &tmap_box, p, S, blockIdx.y, blockIdx.x, -1);
+    } else {
+        // More units than SMs: CTA k (in launch order) takes entry k of the
+        // longest-first order (lpt_order_kernel); past the last unit with
+        // history there is nothing to do.
+        const int k = blockIdx.y * gridDim.x + blockIdx.x;
+        const int2 u = p.lpt_order[k];
+        tmem_held = u.x >= 0 && decode_unit<kRows>(&tmap, &tmap_box, p, S, u.x / p.n_splits, u.x % p.n_splits, u.y);
+    }
+    if (warp == 1 && tmem_held) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(S.tmem_base), "r"(kTmemCols)
                      : "memory");
     }
 }
@@ -815,6 +910,7 @@ cudaError_t launch_tc_decode(const DecodeParams& p, cudaStream_t stream, bool* h
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     static int cc[64][2];
+    static int sms[64];
     static bool cc_ready[64];
     static std::mutex mu;
     {
@@ -825,12 +921,13 @@ cudaError_t launch_tc_decode(const DecodeParams& p, cudaStream_t stream, bool* h
                 return e;
             if ((e = cudaDeviceGetAttribute(&cc[dev][1], cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
                 return e;
-            if ((e = cudaFuncSetAttribute(tc_decode_kernel<12>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)sizeof(Smem) + 1024)) != cudaSuccess)
+            if ((e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
                 return e;
-            if ((e = cudaFuncSetAttribute(tc_decode_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)sizeof(Smem) + 1024)) != cudaSuccess)
-                return e;
+            for (auto fn : {tc_decode_kernel<12, false>, tc_decode_kernel<16, false>, tc_decode_kernel<12, true>,
+                            tc_decode_kernel<16, true>})
+                if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              (int)sizeof(Smem) + 1024)) != cudaSuccess)
+                    return e;
             cc_ready[dev] = true;
         }
     }
@@ -862,6 +959,10 @@ cudaError_t launch_tc_decode(const DecodeParams& p, cudaStream_t stream, bool* h
         if (e == cudaSuccess) *handled = true;
         return e;
     }
+    // More units than SMs (a batch of many, uneven requests): the CTAs take the
+    // units in longest-first order (schedule_units) instead of request order.
+    const long long units = (long long)p.n_splits * p.B;
+    const bool lpt = p.n_splits > 1 && p.B <= kLptMaxB && units > sms[dev];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(p.n_splits), static_cast<unsigned>(p.B));
     cfg.blockDim = dim3(kThreads);
@@ -875,8 +976,20 @@ cudaError_t launch_tc_decode(const DecodeParams& p, cudaStream_t stream, bool* h
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = HT <= 12 ? cudaLaunchKernelEx(&cfg, tc_decode_kernel<12>, map, map_box, q)
-                 : cudaLaunchKernelEx(&cfg, tc_decode_kernel<16>, map, map_box, q);
+    if (lpt) {
+        // the longest-first order, then the decode (a programmatic dependent of it)
+        cudaLaunchConfig_t ocfg = cfg;
+        ocfg.gridDim = dim3(1);
+        ocfg.blockDim = dim3(kLptThreads);
+        ocfg.dynamicSmemBytes = 0;
+        if ((e = cudaLaunchKernelEx(&ocfg, lpt_order_kernel, q)) != cudaSuccess) return e;
+    }
+    if (lpt)
+        e = HT <= 12 ? cudaLaunchKernelEx(&cfg, tc_decode_kernel<12, true>, map, map_box, q)
+                     : cudaLaunchKernelEx(&cfg, tc_decode_kernel<16, true>, map, map_box, q);
+    else
+        e = HT <= 12 ? cudaLaunchKernelEx(&cfg, tc_decode_kernel<12, false>, map, map_box, q)
+                     : cudaLaunchKernelEx(&cfg, tc_decode_kernel<16, false>, map, map_box, q);
     if (e != cudaSuccess) return e;
     e = cudaGetLastError();
     if (e == cudaSuccess) *handled = true;

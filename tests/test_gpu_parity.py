@@ -523,3 +523,91 @@ def test_full_size_dcp_shards_and_merge(L, impl):
     ro, rl = oracle_rows(sc.full, reqs, heads)
     assert_parity(out[reqs][:, :, heads], lse[reqs][:, :, heads], ro, rl, what="merged 142,000")
     assert not torch.isnan(out).any()
+
+
+# ----------------------------------------------------------------------------
+# Longest-first launches of the 12-head kernel (more units than SMs, <= 256
+# requests): each CTA maps its launch index to a rank in the longest-first
+# order of all (request, partition) units, computed on the device from the
+# lengths; units past a request's end write an empty partial
+# ----------------------------------------------------------------------------
+
+def _ragged(seed, B, lo, hi, zeros=0):
+    rng = np.random.default_rng([seed, 23])
+    lens = [int(x) for x in rng.integers(lo, hi, size=B)]
+    for k in range(zeros):
+        lens[(7 * k + 3) % B] = 0
+    return lens
+
+
+@pytest.mark.parametrize("B,H,T,n_splits,zeros", [
+    (20, 12, 1, 12, 0),     # 240 units of up to ~8 pages
+    (64, 12, 1, 0, 5),      # automatic count, empty requests
+    (40, 4, 4, 6, 2),       # 16 rows (causal verify), 240 units
+    (256, 12, 1, 2, 9),     # the largest longest-first batch
+    (257, 12, 1, 2, 0),     # one more request: plain launch
+    (160, 16, 1, 1, 0),     # unsplit: plain launch
+])
+def test_longest_first_launch_matches_oracle(L, impl, B, H, T, n_splits, zeros):
+    lens = _ragged(B + H + T, B, T, 2600, zeros)
+    case = synth.make_decode_case(3000 + B, lens, H, T, extra_pages=2)
+    out, lse = supported(L, impl, case.to("cuda"), n_splits)
+    ro, rl = oracle_full(case)
+    assert_parity(out, lse, ro, rl, what=f"B={B} H={H} T={T} splits={n_splits}")
+
+
+def test_longest_first_launch_repeated_and_replayed(L, impl):
+    """Direct calls in a row and CUDA-graph replays of a longest-first launch all
+    answer correctly (each launch recomputes its order from the lengths)."""
+    lens = _ragged(77, 48, 1, 5000, 3)
+    live = synth.make_decode_case(4001, lens, 12, 1, extra_pages=2).to("cuda")
+    s = torch.cuda.Stream()
+    out = torch.empty((48, 1, 12, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((48, 1, 12), device="cuda")
+
+    def call():
+        L.mla_decode_paged(live.q, live.kv_cache, live.kv_scale, live.block_table, live.seq_lens, 10,
+                           live.sm_scale, out, lse, s)
+
+    ro, rl = oracle_full(synth.make_decode_case(4001, lens, 12, 1, extra_pages=2))
+    for _ in range(3):
+        out.fill_(float("nan"))
+        with torch.cuda.stream(s):
+            call()
+        torch.cuda.synchronize()
+        assert L.mla_device_error() == 0
+        assert_parity(out, lse, ro, rl, what="longest-first launch, direct call")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call()
+    for _ in range(3):
+        out.fill_(float("nan"))
+        with torch.cuda.stream(s):
+            g.replay()
+        torch.cuda.synchronize()
+        assert L.mla_device_error() == 0
+        assert_parity(out, lse, ro, rl, what="longest-first launch, graph replay")
+
+
+def test_longest_first_launch_reports_a_bad_length(L):
+    """A seq_len beyond the block table in a longest-first launch: that request
+    reads nothing (out = 0, lse = -inf) and device error 3 is reported; the
+    other requests are unaffected."""
+    prev = L.mla_set_impl(IMPLS["tcgen05"])
+    try:
+        lens = _ragged(5, 30, 64, 3000)
+        case = synth.make_decode_case(4100, lens, 12, 1)
+        g = case.to("cuda")
+        sl = g.seq_lens.clone()
+        sl[4] = 64 * g.block_table.shape[1] + 5
+        out = torch.full((30, 1, 12, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.full((30, 1, 12), float("nan"), device="cuda")
+        L.mla_decode_paged(g.q, g.kv_cache, g.kv_scale, g.block_table, sl, 8, g.sm_scale, out, lse)
+        torch.cuda.synchronize()
+        assert L.mla_device_error() == 3
+        assert torch.all(out[4] == 0) and torch.all(torch.isneginf(lse[4]))
+        keep = [b for b in range(30) if b != 4]
+        ro, rl = oracle_full(case)
+        assert_parity(out[keep], lse[keep], ro[keep], rl[keep], what="other requests")
+    finally:
+        L.mla_set_impl(prev)

@@ -10,6 +10,7 @@ call really split into several partitions.  This file is collected last so
 that a run stopping at the first failure has run every other test."""
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
@@ -57,9 +58,16 @@ def _resolved_splits(L, case, n_splits):
     return -(-mp // chunk)
 
 
-@pytest.mark.parametrize("name,n_splits", [("tp8_batch", 0), ("verify", 5), ("tiny", 4)])
+def _longest_first_case():
+    """40 requests x 12 heads in 8 partitions: 320 units, more than SMs, so the
+    12-head kernel takes them in longest-first order."""
+    rng = np.random.default_rng(41)
+    return synth.make_decode_case(4200, [int(x) for x in rng.integers(200, 3000, size=40)], 12, 1)
+
+
+@pytest.mark.parametrize("name,n_splits", [("tp8_batch", 0), ("verify", 5), ("tiny", 4), ("longest_first", 8)])
 def test_noalloc_matches_oracle_and_allocating_entry_point_twice(L, name, n_splits):
-    cpu = synth.workload_case(name, reduced=True)
+    cpu = _longest_first_case() if name == "longest_first" else synth.workload_case(name, reduced=True)
     case = cpu.to("cuda")
     n_eff = _resolved_splits(L, case, n_splits)
     assert n_eff > 1, "the case must use the split scratch"
