@@ -45,7 +45,10 @@ def parse():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--sustain-s", type=float, default=2.0,
-                    help="seconds of back-to-back graph replays after the timed steps (clock record)")
+                    help="seconds of back-to-back graph replays after the timed steps (clock record); "
+                         "0 skips them")
+    ap.add_argument("--requests", type=int, default=0,
+                    help="profiling only: keep the first N requests of the workload's batch")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="serving_mix",
                     help="serving_mix (config 5: the ragged batch as the value, the 393,216-position "
@@ -283,9 +286,11 @@ class ClockSampler:
                 "samples": len(rows), "power_w_max": max(pw) if pw else None}
 
 
-def make_inputs(name, device):
+def make_inputs(name, device, requests=0):
+    """The workload's inputs; requests > 0 keeps the first that many requests of
+    its batch (a smaller case of the same shape, for profiler captures)."""
     from mla_latent_kv_fp8_gb300 import synth
-    return synth.workload_case(name, device=device)
+    return synth.workload_case(name, device=device, requests=requests)
 
 
 # Config 5 of the benchmark ("long-context and ragged serving mix"): its ragged
@@ -302,7 +307,7 @@ class DecodeStep:
     def __init__(self, L, name, args, dev, stream):
         import torch
         self.L, self.name, self.dev, self.stream = L, name, dev, stream
-        base = make_inputs(name, "cpu" if name in ("tiny",) else dev).to(dev)
+        base = make_inputs(name, "cpu" if name in ("tiny",) else dev, getattr(args, "requests", 0)).to(dev)
         self.base = base
         self.kv_bytes = base.kv_bytes()
         B, T, H = base.B, base.T, base.H
@@ -326,7 +331,13 @@ class DecodeStep:
         resolved = L.mla_auto_splits(B, T, H, mp, 0) if n_splits == 0 else n_splits
         self.chunk = L.mla_split_chunk_pages(mp, resolved)
         self.n_eff = -(-mp // self.chunk)
-        self.launches_per_step = 1 + (1 if self.n_eff > 1 else 0)
+        # our kernels per step: the decode, the split combine when split, and for a
+        # 12-head tensor-core launch with more units than SMs the longest-first
+        # ordering kernel before the decode
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        lpt = (args.kernel != "simt" and H * T <= 16 and self.n_eff > 1
+               and B <= 1024 and B * self.n_eff > sms)
+        self.launches_per_step = 1 + (1 if self.n_eff > 1 else 0) + (1 if lpt else 0)
         self.graph = None
         self.gsteps = self.n_copies * max(1, -(-16 // self.n_copies))
 
@@ -394,8 +405,10 @@ class DecodeStep:
 
     def sustained(self, seconds, barrier):
         """Graph replays back to back for at least `seconds` (the clocks seen under
-        a long run of this step); returns (us per step, steps)."""
+        a long run of this step); returns (us per step, steps), or (None, 0)."""
         import torch
+        if seconds <= 0:
+            return None, 0
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier()
         ev0.record(self.stream)
@@ -556,6 +569,8 @@ def run_ours(args):
         if args.workload == "serving_mix":
             desc += (" -- part (b) of the long-context and ragged serving mix; part (a), one request at "
                      "393,216 positions, under 'serving_mix'")
+        if getattr(args, "requests", 0):
+            desc += f" [profiling case: first {args.requests} requests only]"
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
@@ -572,10 +587,10 @@ def run_ours(args):
             "direct_calls": {"value": round(job_gbps(kv_bytes, world, ms_direct), 1),
                              "unit": "GB/s", "ms_per_step": round(ms_direct, 5), "steps": kdirect,
                              "note": "one host API call per step, no graph"},
-            "sustained": {"value": round(job_gbps(kv_bytes, world, sus_us * 1e-3), 1), "unit": "GB/s",
-                          "us_per_step": round(sus_us, 3), "steps": sus_steps,
-                          "note": f"graph replays back to back for >= {args.sustain_s:g} s right after the "
-                                  f"timed steps; the clock record covers both"},
+            "sustained": ({"value": round(job_gbps(kv_bytes, world, sus_us * 1e-3), 1), "unit": "GB/s",
+                           "us_per_step": round(sus_us, 3), "steps": sus_steps,
+                           "note": f"graph replays back to back for >= {args.sustain_s:g} s right after the "
+                                   f"timed steps; the clock record covers both"} if sus_steps else None),
             "decode_steps_per_s": round(steps_per_s, 1),
             "model_steps_per_s_attention_only": {
                 "value": round(steps_per_s / MLA_LAYERS, 1), "layers": MLA_LAYERS,

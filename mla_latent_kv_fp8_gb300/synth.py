@@ -398,24 +398,30 @@ WORKLOADS = {
 }
 
 
-def workload_case(name, device="cpu", reduced=False):
-    """Inputs for one named workload; ``reduced`` shrinks contexts for the oracle."""
+def workload_case(name, device="cpu", reduced=False, requests=0):
+    """Inputs for one named workload; ``reduced`` shrinks contexts for the oracle;
+    ``requests`` > 0 keeps the first that many requests of the batch (the same
+    latents for them; a smaller case of the same shape)."""
     seed = WORKLOADS[name][1]
+
+    def first(lens):
+        return lens[:requests] if requests else lens
+
     if name == "tiny":
         return make_decode_case(seed, [1024], 12, 1, device=device)
     if name == "tp8_batch":
         L = 2 * 1024 + 37 if reduced else 32768
-        return make_decode_case(seed, tp8_lens(seed, 8 if not reduced else 3, L), 12, 1, device=device)
+        return make_decode_case(seed, first(tp8_lens(seed, 8 if not reduced else 3, L)), 12, 1, device=device)
     if name == "verify":
         lens = verify_lens(seed, 4, 300, 1400) if reduced else verify_lens(seed)
-        return make_decode_case(seed, lens, 12, 4, device=device)
+        return make_decode_case(seed, first(lens), 12, 4, device=device)
     if name == "long":
         L = 20000 + 13 if reduced else 393216
         return make_decode_case(seed, [L], 12, 1, device=device)
     if name == "dcp_shard":  # one DCP shard as decoded locally: out + lse over its positions
         L = 300 + 11 if reduced else 17750
-        return make_decode_case(seed, [L] * (2 if reduced else 32), 96, 1, device=device)
+        return make_decode_case(seed, first([L] * (2 if reduced else 32)), 96, 1, device=device)
     if name == "ragged":
         lens = ragged_lens(seed, 16, 64, 3000) if reduced else ragged_lens(seed)
-        return make_decode_case(seed, lens, 12, 1, device=device)
+        return make_decode_case(seed, first(lens), 12, 1, device=device)
     raise KeyError(name)

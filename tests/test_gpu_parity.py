@@ -526,10 +526,10 @@ def test_full_size_dcp_shards_and_merge(L, impl):
 
 
 # ----------------------------------------------------------------------------
-# Longest-first launches of the 12-head kernel (more units than SMs, <= 256
-# requests): each CTA maps its launch index to a rank in the longest-first
-# order of all (request, partition) units, computed on the device from the
-# lengths; units past a request's end write an empty partial
+# Longest-first launches of the 12-head kernel (more units than SMs, <= 1,024
+# requests): a one-CTA kernel orders all (request, partition) units longest
+# first from the device-resident lengths and writes the empty partials; decode
+# CTA k takes entry k of that order
 # ----------------------------------------------------------------------------
 
 def _ragged(seed, B, lo, hi, zeros=0):
@@ -540,16 +540,17 @@ def _ragged(seed, B, lo, hi, zeros=0):
     return lens
 
 
-@pytest.mark.parametrize("B,H,T,n_splits,zeros", [
-    (20, 12, 1, 12, 0),     # 240 units of up to ~8 pages
-    (64, 12, 1, 0, 5),      # automatic count, empty requests
-    (40, 4, 4, 6, 2),       # 16 rows (causal verify), 240 units
-    (256, 12, 1, 2, 9),     # the largest longest-first batch
-    (257, 12, 1, 2, 0),     # one more request: plain launch
-    (160, 16, 1, 1, 0),     # unsplit: plain launch
+@pytest.mark.parametrize("B,H,T,n_splits,zeros,hi", [
+    (20, 12, 1, 12, 0, 2600),    # 240 units of up to ~8 pages
+    (64, 12, 1, 0, 5, 2600),     # automatic count, empty requests
+    (40, 4, 4, 6, 2, 2600),      # 16 rows (causal verify), 240 units
+    (256, 12, 1, 2, 9, 2600),
+    (1024, 12, 1, 2, 30, 500),   # the largest longest-first batch
+    (1025, 12, 1, 2, 0, 500),    # one more request: request order
+    (160, 16, 1, 1, 0, 2600),    # unsplit: one CTA per request
 ])
-def test_longest_first_launch_matches_oracle(L, impl, B, H, T, n_splits, zeros):
-    lens = _ragged(B + H + T, B, T, 2600, zeros)
+def test_longest_first_launch_matches_oracle(L, impl, B, H, T, n_splits, zeros, hi):
+    lens = _ragged(B + H + T, B, T, hi, zeros)
     case = synth.make_decode_case(3000 + B, lens, H, T, extra_pages=2)
     out, lse = supported(L, impl, case.to("cuda"), n_splits)
     ro, rl = oracle_full(case)
