@@ -78,3 +78,16 @@ cudaError_t launch_stream_probe(const uint8_t* kv, int64_t num_pages, const int3
                                 int pages_per_cta, int* err, cudaStream_t stream);
 
 }  // namespace mla
+
+// ---------------------------------------------------------------- host side
+// Host-only declarations that need the driver API types.
+#include <cuda.h>
+
+namespace mla {
+
+// The two TMA views of the cache that the tensor-core kernels copy pages
+// through: map3 moves a whole 64-position page per copy, map2 one 64 x 64-byte
+// box of it (both 64-byte swizzled).
+cudaError_t encode_cache_maps(CUtensorMap* map3, CUtensorMap* map2, const uint8_t* kv, int64_t num_pages);
+
+}  // namespace mla

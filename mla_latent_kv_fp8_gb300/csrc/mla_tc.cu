@@ -835,7 +835,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- host side
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+}  // namespace
+
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
     std::call_once(once, [] {
@@ -885,8 +887,6 @@ cudaError_t encode_cache_maps(CUtensorMap* map3, CUtensorMap* map2, const uint8_
     }
     return cudaSuccess;
 }
-
-}  // namespace
 
 cudaError_t launch_tc_wide(const DecodeParams& p, const CUtensorMap& map, const CUtensorMap& map_box,
                            cudaStream_t stream);
