@@ -355,6 +355,50 @@ def test_graph_survives_a_later_larger_call(L):
     assert_parity(out, lse, ro, rl, what="graph replayed after the stream's scratch grew")
 
 
+def test_release_graph_scratch_frees_what_captures_kept(L):
+    """mla_release_graph_scratch frees the split scratch that captured calls used:
+    the buffer a later growth retired and the one still attached to the stream.
+    Once the graphs are destroyed, the device's free memory grows by about those
+    bytes, the stream keeps working (its next call allocates anew) and a second
+    release has nothing to do."""
+    s = torch.cuda.Stream()
+    small = synth.make_decode_case(99, [4096] * 4, 128, 1).to("cuda")   # 64 one-page partitions
+    big = synth.make_decode_case(98, [16384] * 4, 128, 1).to("cuda")    # 256
+    out = torch.empty((4, 1, 128, 512), dtype=torch.bfloat16, device="cuda")
+    with torch.cuda.stream(s):
+        _one_page_partitions(L, small, s, out, None)
+    torch.cuda.synchronize()
+    g1 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g1, stream=s):
+        _one_page_partitions(L, small, s, out, None)
+    with torch.cuda.stream(s):  # grows the scratch: the captured buffer is retired
+        _one_page_partitions(L, big, s, out, None)
+    torch.cuda.synchronize()
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g2, stream=s):  # the new buffer is now a graph's too
+        _one_page_partitions(L, big, s, out, None)
+    torch.cuda.synchronize()
+    assert L.mla_device_error() == 0
+    del g1, g2
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    L.mla_release_graph_scratch()
+    torch.cuda.synchronize()
+    free1 = torch.cuda.mem_get_info()[0]
+    kept = 1.25 * (L.mla_decode_workspace_bytes(4, 1, 128, 64) + L.mla_decode_workspace_bytes(4, 1, 128, 256))
+    assert free1 - free0 >= 0.5 * kept, (free0, free1, kept)
+    lse = torch.empty((4, 1, 128), device="cuda")
+    out.fill_(float("nan"))
+    with torch.cuda.stream(s):
+        L.mla_decode_paged(small.q, small.kv_cache, small.kv_scale, small.block_table, small.seq_lens, 5,
+                           small.sm_scale, out, lse, s)
+    torch.cuda.synchronize()
+    assert L.mla_device_error() == 0
+    ro, rl = oracle_full(small)
+    assert_parity(out, lse, ro, rl, what="decode on a stream whose graph scratch was released")
+    L.mla_release_graph_scratch()
+
+
 def test_two_streams_at_once(L, impl):
     """Calls on two streams run concurrently with their own split scratch."""
     cases = [synth.make_decode_case(81 + k, [3000, 900], 12, 1).to("cuda") for k in range(2)]

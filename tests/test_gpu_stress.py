@@ -3,7 +3,7 @@ into their hard regimes, element by element against the FP64 oracle.
 
 The tcgen05 kernels take each row's probabilities against a lazy reference
 maximum (moved, with an in-place rescale of the accumulated output in tensor
-memory, only when a score would exceed it by 8 log2 units), store them as two
+memory, only when a score would exceed it by 8.8 log2 units), store them as two
 e4m3 terms, and split the query into two exact e4m3 terms.  N(0,1) inputs give
 flat softmaxes that rarely move the reference, so these cases plant structure
 (mla_latent_kv_fp8_gb300.synth stress patterns):
