@@ -306,6 +306,13 @@ mla_status_t internal_launch_decode(DecodeParams& p, cudaStream_t s) {
         m.out = p.out;
         m.lse = p.lse;
         m.pdl = 1;
+        // partitions past a request's history are not written (the longest-first
+        // launch never visits them): the combine counts them as empty
+        m.seq_lens = p.seq_lens;
+        m.rows_per_req = p.T * p.H;
+        m.T = p.T;
+        m.chunk_pages = p.chunk_pages;
+        m.max_pages = p.max_pages;
         e = launch_merge(m, s);
         if (e != cudaSuccess) return cuda_fail(e, "split combine launch");
     }

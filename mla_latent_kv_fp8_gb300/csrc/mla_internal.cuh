@@ -69,6 +69,15 @@ struct MergeParams {
     uint16_t* out;              // bf16 [rows][512]
     float* lse;                 // [rows] or null
     int pdl;                    // launched as a programmatic dependent of the producer
+    // The split combine of a decode call sets these (null seq_lens otherwise):
+    // part s of request b's rows holds an answer only for the partitions its
+    // history reaches, s < ceil(ceil(L_b / 64) / chunk_pages); the others were
+    // not written by this call and count as empty, whatever the scratch holds.
+    const int32_t* seq_lens;    // [rows / rows_per_req], device
+    int rows_per_req;           // H * T
+    int T;
+    int chunk_pages;
+    int max_pages;              // lengths beyond max_pages * 64 (or below T) count as 0
 };
 
 cudaError_t launch_simt_decode(const DecodeParams& p, cudaStream_t stream);

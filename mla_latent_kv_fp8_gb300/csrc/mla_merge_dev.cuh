@@ -30,6 +30,18 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Parts of `row` that hold an answer: all p.S of them, or in a decode's split
+// combine only the partitions that the row's request reaches (its length read
+// and checked as the decode kernels do).
+__device__ __forceinline__ int live_parts(const MergeParams& p, int64_t row) {
+    if (!p.seq_lens) return p.S;
+    int L = __ldg(p.seq_lens + row / p.rows_per_req);
+    if (L < 0 || L > p.max_pages * kPage || (L > 0 && L < p.T)) L = 0;
+    const int pages = (L + kPage - 1) / kPage;
+    const int n = (pages + p.chunk_pages - 1) / p.chunk_pages;
+    return n < p.S ? n : p.S;
+}
+
 template <bool kBf16In>
 __device__ __forceinline__ float load1(const void* base, int64_t idx) {
     if constexpr (kBf16In) {
@@ -55,11 +67,13 @@ __device__ __forceinline__ float2 load2(const void* base, int64_t idx) {
 template <bool kBf16In>
 __device__ __forceinline__ void merge_warp(const MergeParams& p, int64_t row, int chunk, int lane) {
     const int64_t col = (int64_t)chunk * 64 + lane * 2;
-    const float ls = (lane < p.S) ? p.part_lse[(int64_t)lane * p.rows + row] : -INFINITY;
+    const int live = live_parts(p, row);  // loaded beside the normalisers, not before them
+    float ls = (lane < p.S) ? p.part_lse[(int64_t)lane * p.rows + row] : -INFINITY;
     float2 v[32];
 #pragma unroll
     for (int s = 0; s < 32; ++s)
         v[s] = s < p.S ? load2<kBf16In>(p.part_out, ((int64_t)s * p.rows + row) * kDv + col) : make_float2(0.f, 0.f);
+    if (lane >= live) ls = -INFINITY;
     const float M = warp_max(ls);
     uint16_t* dst = p.out + row * kDv + col;
     if (M == -INFINITY) {
@@ -134,11 +148,13 @@ __device__ __forceinline__ void merge_row(const MergeParams& p, int64_t row, int
     // The first round's values are requested together with the normalisers,
     // before the weights are known (every part s < S lies inside the buffer);
     // a part of weight 0 among them is loaded but never multiplied.
-    const float ls = (lane < p.S) ? p.part_lse[(int64_t)lane * p.rows + row] : -INFINITY;
+    const int live = live_parts(p, row);  // loaded beside the normalisers, not before them
+    float ls = (lane < p.S) ? p.part_lse[(int64_t)lane * p.rows + row] : -INFINITY;
     uint4 v[kR][kVecs];
 #pragma unroll
     for (int j = 0; j < kR; ++j)
         if (j < p.S) load_part(j, v[j]);
+    if (lane >= live) ls = -INFINITY;
     const float M = warp_max(ls);
     uint4* dst = reinterpret_cast<uint4*>(p.out + row * kDv + 16 * lane);
     if (M == -INFINITY) {
@@ -207,6 +223,7 @@ __device__ __forceinline__ void merge_cta(const MergeParams& p, int64_t row, int
     const int lane = tid & 31, wid = tid >> 5;
     const int col = chunk * 32 + lane;
     float m_w = -INFINITY, l_w = 0.f, acc = 0.f;
+    const int live = live_parts(p, row);
     for (int base = 0; base < p.S; base += 256) {
         float v[32];
 #pragma unroll
@@ -215,7 +232,8 @@ __device__ __forceinline__ void merge_cta(const MergeParams& p, int64_t row, int
             v[k] = s < p.S ? load1<kBf16In>(p.part_out, ((int64_t)s * p.rows + row) * kDv + col) : 0.f;
         }
         const int sl = base + wid + 8 * lane;  // this lane's part for the normalisers
-        const float ls = sl < p.S ? p.part_lse[(int64_t)sl * p.rows + row] : -INFINITY;
+        float ls = sl < p.S ? p.part_lse[(int64_t)sl * p.rows + row] : -INFINITY;
+        if (sl >= live) ls = -INFINITY;
         const float mr = warp_max(ls);
         if (mr == -INFINITY) continue;  // warp-uniform: no part of this round counts
         const float mn = fmaxf(m_w, mr);

@@ -146,9 +146,10 @@ __device__ __forceinline__ void split_p(float a0, float a1, uint32_t& c1, uint32
 // are dispatched in launch order, so the SMs that free up take the longest
 // units left and end within about one short unit of each other.  Entry k is
 // {b * n_splits + split, seq_len of b}, or {-1, 0} past the last unit with
-// history.  The empty units (partitions past a request's end) get their empty
-// partial (lse = -inf) here; a length outside [0, 64 * max_pages], or in
-// (0, T), reads nothing and sets device error 3.
+// history.  Nothing is written for the empty units (partitions past a
+// request's end): the split combine counts the partitions past a request's
+// history as empty.  A length outside [0, 64 * max_pages], or in (0, T),
+// reads nothing and sets device error 3.
 __global__ void __launch_bounds__(kLptThreads, 1) lpt_order_kernel(const DecodeParams p) {
     __shared__ int full_pfx[kLptMaxB + 1];
     __shared__ int rem_s[kLptMaxB];
@@ -156,7 +157,7 @@ __global__ void __launch_bounds__(kLptThreads, 1) lpt_order_kernel(const DecodeP
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");  // they wait for this grid to finish
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int B = p.B, chunk = p.chunk_pages, n_splits = p.n_splits, HT = p.H * p.T;
+    const int B = p.B, chunk = p.chunk_pages, n_splits = p.n_splits;
     int L = 0, full = 0, rem = 0;
     if (tid < B) {
         L = __ldg(p.seq_lens + tid);
@@ -204,8 +205,6 @@ __global__ void __launch_bounds__(kLptThreads, 1) lpt_order_kernel(const DecodeP
             }
             order[n_full + ahead] = make_int2(tid * n_splits + full, L);
         }
-        for (int sp = full + (rem > 0 ? 1 : 0); sp < n_splits; ++sp)
-            for (int r = 0; r < HT; ++r) p.part_lse[((int64_t)sp * B + tid) * HT + r] = -INFINITY;
     }
     for (int k = n_full + n_part + tid; k < B * n_splits; k += kLptThreads) order[k] = make_int2(-1, 0);
 }

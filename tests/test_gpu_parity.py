@@ -634,6 +634,33 @@ def test_longest_first_launch_repeated_and_replayed(L, impl):
         assert_parity(out, lse, ro, rl, what="longest-first launch, graph replay")
 
 
+def test_split_combine_ignores_partitions_past_each_history(L, impl):
+    """The split combine counts a request's partitions past its history as empty
+    whatever the scratch holds (a longest-first launch never writes them): a
+    call whose requests are all long fills every partition of the stream's
+    scratch with real partials, and the next call of the same shape on that
+    stream, with mostly short requests, still answers exactly."""
+    B, H, n_splits, hi = 48, 12, 10, 5120
+    s = torch.cuda.Stream()
+    full = synth.make_decode_case(4200, [hi] * B, H, 1).to("cuda")
+    lens = [hi] + [int(x) for x in np.random.default_rng(4201).integers(1, 700, B - 1)]
+    short = synth.make_decode_case(4202, lens, H, 1)
+    g = short.to("cuda")
+    assert g.block_table.shape == full.block_table.shape
+    out = torch.empty((B, 1, H, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, 1, H), device="cuda")
+    with torch.cuda.stream(s):
+        L.mla_decode_paged(full.q, full.kv_cache, full.kv_scale, full.block_table, full.seq_lens, n_splits,
+                           full.sm_scale, out, lse, s)
+        out.fill_(float("nan"))
+        L.mla_decode_paged(g.q, g.kv_cache, g.kv_scale, g.block_table, g.seq_lens, n_splits, g.sm_scale, out,
+                           lse, s)
+    torch.cuda.synchronize()
+    assert L.mla_device_error() == 0
+    ro, rl = oracle_full(short)
+    assert_parity(out, lse, ro, rl, what="short requests after long ones on the same scratch")
+
+
 def test_longest_first_launch_reports_a_bad_length(L):
     """A seq_len beyond the block table in a longest-first launch: that request
     reads nothing (out = 0, lse = -inf) and device error 3 is reported; the
