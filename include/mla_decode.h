@@ -238,16 +238,20 @@ MLA_API mla_status_t mla_append_latent(const mla_tensor_t *latent, const float *
 MLA_API int32_t mla_auto_splits(int32_t B, int32_t T, int32_t H, int32_t max_pages, int32_t sm_count);
 
 /* The split count for a batch whose lengths the caller knows on the host (a
- * serving engine schedules them): pass the result as n_splits.  For units of
- * more than 16 rows (the 32-row tensor-core kernel, where a partition costs
- * its pages at a fixed per-page time plus a fixed set-up and epilogue) it
- * replays the launch of the (request, partition, row-CTA) grid on the host:
- * CTAs in launch order, each on the SM that frees first, one per SM, each
- * costing its pages plus 8, and returns the count with the shortest
- * finish (ties: fewer partitions), trying counts up to 8 waves of full-length
- * CTAs.  For units of up to 16 rows (HBM-bound, one wave), or when
- * host_seq_lens is NULL, it returns mla_auto_splits(B, T, H, max_pages,
- * sm_count).
+ * serving engine schedules them): pass the result as n_splits.  It replays
+ * the launch on the host -- each CTA on the SM that frees first, one per SM,
+ * a partition costing its pages at a fixed per-page time plus a fixed 8 pages
+ * of set-up and epilogue -- and returns the count with the shortest finish
+ * (ties: fewer partitions).  Units of more than 16 rows (the 32-row
+ * tensor-core kernel, ceil(H * T / 32) CTAs per unit) run in launch order.
+ * Units of up to 16 rows run one CTA each: in launch order while they fit the
+ * SMs, and otherwise (up to 1,024 requests) longest first -- full partitions,
+ * then the partial ones by length, then those past each request's history at
+ * ~3/4 page each -- as the decode launches them.  Counts are tried up to 8
+ * waves of full-length CTAs, and for units of up to 16 rows down to
+ * partitions of 64 pages.  When host_seq_lens is NULL (or B is 0) it returns
+ * mla_auto_splits(B, T, H, max_pages, sm_count).  A plan takes ~0.1-2 ms on
+ * one host core, so an engine plans once per batch.
  *   host_seq_lens  host pointer to the B lengths the decode will read from
  *                  seq_lens (values outside [0, 64 * max_pages] are clamped).
  *   max_pages      the block table's width, as passed to the decode.

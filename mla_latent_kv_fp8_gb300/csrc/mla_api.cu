@@ -385,18 +385,25 @@ int32_t mla_auto_splits(int32_t B, int32_t T, int32_t H, int32_t max_pages, int3
     return (int32_t)ceil_div(max_pages, chunk);
 }
 
-// Per-CTA fixed cost of a partition in the length-aware plan, in pages of
-// loop time: set-up (~3 us) and epilogue (~2.4 us) of a 32-row CTA against
-// ~0.7 us per page.
-constexpr int64_t kPlanFixedPages = 8;
+// Costs of the length-aware plan, in eighths of a page of loop time (~0.74 us
+// per page under a full wave): a partition costs its pages plus a fixed 8
+// pages per CTA (set-up ~3-4.5 us and epilogue ~2-2.4 us); a CTA whose
+// partition lies past its request's history costs ~0.75 page in a
+// longest-first launch, where it still starts after all the others.
+constexpr int64_t kPlanPage = 8;
+constexpr int64_t kPlanFixed = 8 * kPlanPage;
+constexpr int64_t kPlanEmpty = 6;
+// The 12-head kernel orders the units of at most this many requests longest
+// first when they outnumber the SMs (its ordering kernel's limit).
+constexpr int32_t kLongestFirstMaxBatch = 1024;
 
 int32_t mla_plan_splits(int32_t B, int32_t T, int32_t H, const int32_t* host_seq_lens, int32_t max_pages,
                         int32_t sm_count) {
     const int32_t fallback = mla_auto_splits(B, T, H, max_pages, sm_count);
     if (!host_seq_lens || B <= 0 || max_pages <= 2) return fallback;
     const int64_t rows = (int64_t)(T > 0 ? T : 1) * (H > 0 ? H : 1);
-    if (rows <= 16) return fallback;  // HBM-bound kernel: one wave, lengths do not change it
-    const int64_t G = ceil_div(rows, 32);
+    const bool narrow = rows <= 16;  // the 12-head kernel: one CTA per unit
+    const int64_t G = narrow ? 1 : ceil_div(rows, 32);
     if (sm_count <= 0) {
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -411,13 +418,16 @@ int32_t mla_plan_splits(int32_t B, int32_t T, int32_t H, const int32_t* host_seq
         L = L < 0 ? 0 : (L > (int64_t)max_pages * kPage ? (int64_t)max_pages * kPage : L);
         pages[b] = ceil_div(L, kPage);
     }
-    // Candidate counts: up to 8 waves of CTAs at full length (more never pays),
-    // one per distinct chunk size.  Each has a lower bound on its finish (its
-    // longest CTA, and its total work spread over every SM); candidates are
-    // replayed in the order of that bound until the bound passes the best
-    // finish found, which gives the same answer as replaying them all.
+    // Candidate counts: up to 8 waves of CTAs at full length (more never pays)
+    // and, for the 12-head kernel, partitions down to 64 pages (a batch of
+    // uneven lengths leaves most of its units empty); one per distinct chunk
+    // size.  Each has a lower bound on its finish (its longest CTA, and its
+    // total work spread over every SM); candidates are replayed in the order
+    // of that bound until the bound passes the best finish found, which gives
+    // the same answer as replaying them all.
     const int64_t most = ceil_div(max_pages, 2);
     int64_t hi = (8 * (int64_t)sm_count) / (B * G);
+    if (narrow) hi = std::max<int64_t>(hi, ceil_div(max_pages, 64));
     hi = hi < 1 ? 1 : (hi > most ? most : hi);
     if (hi > 1024) hi = 1024;
     const int64_t longest = *std::max_element(pages.begin(), pages.end());
@@ -430,29 +440,50 @@ int32_t mla_plan_splits(int32_t B, int32_t T, int32_t H, const int32_t* host_seq
         if (chunk == last_chunk) continue;  // the same snapped plan as a smaller count
         last_chunk = chunk;
         int64_t work = 0;
-        for (int64_t p : pages) work += p + ceil_div(p, chunk) * kPlanFixedPages;
-        const int64_t bound = std::max(std::min(chunk, longest) + kPlanFixedPages, ceil_div(G * work, sm_count));
+        for (int64_t p : pages) work += kPlanPage * p + ceil_div(p, chunk) * kPlanFixed;
+        const int64_t bound =
+            std::max(kPlanPage * std::min(chunk, longest) + kPlanFixed, ceil_div(G * work, sm_count));
         cands.push_back({bound, ceil_div(max_pages, chunk), chunk});
     }
     std::sort(cands.begin(), cands.end(),
               [](const Cand& a, const Cand& b) { return a.bound != b.bound ? a.bound < b.bound : a.n < b.n; });
-    std::vector<int64_t> load((size_t)sm_count);
+    std::vector<int64_t> load((size_t)sm_count), partial;
     int64_t best_cost = -1, best = 1;
     for (const Cand& cd : cands) {
         if (best_cost >= 0 && (cd.bound > best_cost || (cd.bound == best_cost && cd.n > best))) break;
-        // CTAs start in launch order (partition and row-CTA fastest, then the
-        // request), each on the SM that frees first, one CTA per SM.
+        // Each CTA starts on the SM that frees first, one CTA per SM.
         std::fill(load.begin(), load.end(), 0);  // all zero: already a heap
         int64_t cost = 0;                         // the latest finish so far
-        for (int32_t b = 0; b < B; ++b) {
-            for (int64_t sp = 0; sp < cd.n; ++sp) {
-                const int64_t w = std::min(cd.chunk, pages[b] - sp * cd.chunk);
-                if (w <= 0) break;  // partitions past the request's end exit at once
-                for (int64_t r = 0; r < G; ++r) {
-                    std::pop_heap(load.begin(), load.end(), std::greater<int64_t>());
-                    load.back() += w + kPlanFixedPages;
-                    cost = std::max(cost, load.back());
-                    std::push_heap(load.begin(), load.end(), std::greater<int64_t>());
+        auto place = [&](int64_t w) {
+            std::pop_heap(load.begin(), load.end(), std::greater<int64_t>());
+            load.back() += w;
+            cost = std::max(cost, load.back());
+            std::push_heap(load.begin(), load.end(), std::greater<int64_t>());
+        };
+        const bool longest_first =
+            narrow && cd.n > 1 && B <= kLongestFirstMaxBatch && (int64_t)B * cd.n > sm_count;
+        if (longest_first) {
+            // full chunks request by request, then the partial chunks by length,
+            // then the CTAs of the partitions past each history
+            int64_t live = 0;
+            partial.clear();
+            for (int32_t b = 0; b < B; ++b) {
+                const int64_t f = pages[b] / cd.chunk, r = pages[b] - f * cd.chunk;
+                for (int64_t i = 0; i < f; ++i) place(kPlanPage * cd.chunk + kPlanFixed);
+                live += f;
+                if (r > 0) partial.push_back(r);
+            }
+            std::sort(partial.begin(), partial.end(), std::greater<int64_t>());
+            for (int64_t r : partial) place(kPlanPage * r + kPlanFixed);
+            live += (int64_t)partial.size();
+            for (int64_t e = live; e < (int64_t)B * cd.n; ++e) place(kPlanEmpty);
+        } else {
+            // launch order: partition and row-CTA fastest, then the request
+            for (int32_t b = 0; b < B; ++b) {
+                for (int64_t sp = 0; sp < cd.n; ++sp) {
+                    const int64_t w = std::min(cd.chunk, pages[b] - sp * cd.chunk);
+                    if (w <= 0) break;  // partitions past the request's end exit at once
+                    for (int64_t r = 0; r < G; ++r) place(kPlanPage * w + kPlanFixed);
                 }
             }
         }

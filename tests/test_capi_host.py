@@ -247,6 +247,8 @@ def test_auto_splits_invariants_over_a_sweep(L):
     (16, 4, 12, 1568),   # verify-like, 48 rows
     (16, 1, 48, 195),    # a DCP-verify shard before the last
     (3, 2, 64, 700),     # 128 rows, 4 CTAs per unit
+    (8, 1, 12, 512),     # tp8_batch: one wave of 12-head units
+    (1, 1, 12, 6144),    # the 393,216-position request
 ])
 def test_plan_splits_equals_auto_when_every_request_is_full(L, B, T, H, max_pages):
     """With every request max_pages long the length-aware plan and the automatic
@@ -256,12 +258,31 @@ def test_plan_splits_equals_auto_when_every_request_is_full(L, B, T, H, max_page
 
 
 def test_plan_splits_falls_back_to_auto(L):
+    """Without host lengths (or requests) the plan is the automatic count."""
     lens = [1000, 20000, 5, 0, 70000, 3000, 64, 9000]
     mp = -(-max(lens) // 64)
-    for T, H in ((1, 12), (1, 16), (2, 8)):  # units of at most 16 rows: one HBM-bound wave
-        assert L.mla_plan_splits(8, T, H, lens, mp, 152) == L.mla_auto_splits(8, T, H, mp, 152)
-    assert L.lib().mla_plan_splits(8, 4, 12, None, mp, 152) == L.mla_auto_splits(8, 4, 12, mp, 152)
-    assert L.mla_plan_splits(0, 4, 12, [], mp, 152) == L.mla_auto_splits(0, 4, 12, mp, 152)
+    for T, H in ((1, 12), (1, 16), (2, 8), (4, 12)):
+        assert L.lib().mla_plan_splits(8, T, H, None, mp, 152) == L.mla_auto_splits(8, T, H, mp, 152)
+        assert L.mla_plan_splits(0, T, H, [], mp, 152) == L.mla_auto_splits(0, T, H, mp, 152)
+
+
+def test_plan_splits_for_uneven_12_head_batches(L):
+    """12-head units: one wave while the units fit the SMs, and past that the
+    longest-first launch.  An uneven batch of 8 takes short partitions so that
+    its longest request spreads over the SMs its short ones leave free; the
+    seeded 128-request ragged mix takes 5 partitions: the fastest count of a
+    sweep on GB300 (342.2 us per step, against 343.7 at 10, 349.5 at 15,
+    357.3 at the automatic 14, 369.5 at 4, 385.0 at 8)."""
+    lens = [1000, 20000, 5, 0, 70000, 3000, 64, 9000]
+    mp = -(-max(lens) // 64)
+    n = L.mla_plan_splits(8, 1, 12, lens, mp, 152)
+    assert n > L.mla_auto_splits(8, 1, 12, mp, 152)
+    chunk = L.mla_split_chunk_pages(mp, n)
+    assert sum(-(-(-(-x // 64)) // chunk) for x in lens) <= 152  # still one wave
+    ragged = synth.ragged_lens(6)
+    mp = -(-max(ragged) // 64)
+    assert L.mla_plan_splits(128, 1, 12, ragged, mp, 152) == 5
+    assert L.mla_auto_splits(128, 1, 12, mp, 152) == 14
 
 
 def test_plan_splits_ragged_batches(L):
@@ -300,14 +321,22 @@ def test_plan_splits_is_a_valid_plan_over_a_sweep(L):
 
 def _plan_by_replay(B, T, H, lens, max_pages, sm):
     """The length-aware plan written out plainly: every candidate count (one per
-    distinct chunk size, up to 8 full-length waves) replayed in launch order on
-    a min-heap of SM finish times; the earliest finish wins, ties to fewer
+    distinct chunk size, up to 8 full-length waves, and for units of at most
+    16 rows partitions down to 64 pages) replayed on a min-heap of SM finish
+    times, in eighths of a page: a partition costs 8 per page plus 64, in launch
+    order; a 12-head launch of more units than SMs (at most 1,024 requests) runs
+    full chunks first, then partial chunks longest first, then the partitions
+    past each history at 6 each.  The earliest finish wins, ties to fewer
     partitions."""
     import heapq
-    G = -(-(T * H) // 32)
+    narrow = T * H <= 16
+    G = 1 if narrow else -(-(T * H) // 32)
     pages = [-(-min(max(x, 0), 64 * max_pages) // 64) for x in lens]
     most = -(-max_pages // 2)
-    hi = max(1, min(most, (8 * sm) // (B * G), 1024))
+    hi = (8 * sm) // (B * G)
+    if narrow:
+        hi = max(hi, -(-max_pages // 64))
+    hi = max(1, min(most, hi, 1024))
     best = None
     seen = set()
     for c in range(1, hi + 1):
@@ -318,27 +347,45 @@ def _plan_by_replay(B, T, H, lens, max_pages, sm):
         n = -(-max_pages // chunk)
         heap = [0] * sm
         finish = 0
-        for p in pages:
-            for s in range(n):
-                w = min(chunk, p - s * chunk)
-                if w <= 0:
-                    break
-                for _ in range(G):
-                    t = heapq.heappop(heap) + w + 8
-                    finish = max(finish, t)
-                    heapq.heappush(heap, t)
+
+        def place(w):
+            nonlocal finish
+            t = heapq.heappop(heap) + w
+            finish = max(finish, t)
+            heapq.heappush(heap, t)
+
+        if narrow and n > 1 and B <= 1024 and B * n > sm:
+            full = [chunk] * sum(p // chunk for p in pages)
+            part = sorted((p % chunk for p in pages if p % chunk), reverse=True)
+            for w in full + part:
+                place(8 * w + 64)
+            for _ in range(B * n - len(full) - len(part)):
+                place(6)
+        else:
+            for p in pages:
+                for s in range(n):
+                    w = min(chunk, p - s * chunk)
+                    if w <= 0:
+                        break
+                    for _ in range(G):
+                        place(8 * w + 64)
         if best is None or (finish, n) < best:
             best = (finish, n)
     return best[1]
 
 
 def test_plan_splits_matches_a_plain_replay(L):
-    """The library's pruned search returns what replaying every candidate returns."""
+    """The library's pruned search returns what replaying every candidate returns,
+    for the 32-row kernel and for 12-head units (one wave and longest-first)."""
     rng = np.random.default_rng(11)
-    for _ in range(60):
-        B = int(rng.integers(1, 40))
+    for i in range(90):
         T = int(rng.choice([1, 2, 4]))
-        H = int(rng.integers(17 // T + 1, 128 // T + 1))  # more than 16 rows
+        if i % 3 == 2:  # at most 16 rows, batches up to past the longest-first limit
+            B = int(rng.choice([int(rng.integers(1, 40)), int(rng.integers(100, 300)), 1030]))
+            H = int(rng.integers(1, 16 // T + 1))
+        else:
+            B = int(rng.integers(1, 40))
+            H = int(rng.integers(17 // T + 1, 128 // T + 1))  # more than 16 rows
         lens = [int(x) for x in rng.integers(0, int(rng.choice([3000, 40000, 150000])), size=B)]
         mp = max(3, -(-max(lens) // 64))
         sm = int(rng.choice([148, 152]))

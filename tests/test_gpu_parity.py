@@ -535,18 +535,26 @@ FULL = {
 
 @pytest.mark.parametrize("name", sorted(FULL))
 def test_full_size_sampled_rows(L, impl, name):
+    """Each full-size workload at the count the benchmark plans from the host
+    lengths (mla_plan_splits) and at the automatic count, where they differ."""
     case = synth.workload_case(name, device="cuda")
-    n_splits = 4 if name == "tiny" else 0
-    out, lse = supported(L, impl, case, n_splits)
+    if name == "tiny":
+        counts = [4]
+    else:
+        mp = case.block_table.shape[1]
+        counts = sorted({L.mla_plan_splits(case.B, case.T, case.H, case.lens, mp, 0),
+                         L.mla_auto_splits(case.B, case.T, case.H, mp, 0)})
     reqs, heads = FULL[name]
     if reqs is None:  # shortest, longest and one in between
         order = np.argsort(case.lens)
         reqs = sorted({int(order[0]), int(order[len(order) // 2]), int(order[-1])})
     ro, rl = oracle_rows(case, reqs, heads)
-    o = out[reqs][:, :, heads]
-    l = lse[reqs][:, :, heads]
-    assert_parity(o, l, ro, rl, what=f"full {name}/{impl}")
-    assert not torch.isnan(out).any() and not torch.isnan(lse).any()
+    for n_splits in counts:
+        out, lse = supported(L, impl, case, n_splits)
+        o = out[reqs][:, :, heads]
+        l = lse[reqs][:, :, heads]
+        assert_parity(o, l, ro, rl, what=f"full {name}/{impl} splits={n_splits}")
+        assert not torch.isnan(out).any() and not torch.isnan(lse).any()
 
 
 def test_full_size_dcp_shards_and_merge(L, impl):
