@@ -642,6 +642,24 @@ def test_longest_first_launch_repeated_and_replayed(L, impl):
         assert_parity(out, lse, ro, rl, what="longest-first launch, graph replay")
 
 
+@pytest.mark.parametrize("lens", [
+    [1000, 20000, 5, 0, 70000, 3000, 64, 9000],  # one wave of many short partitions
+    "ragged32",                                   # a longest-first launch
+])
+def test_planned_split_counts_match_oracle(L, impl, lens):
+    """The counts mla_plan_splits picks for uneven 12-head batches (85 partitions
+    of 13 pages in one wave for the first; a multi-wave longest-first launch for
+    the second) answer like the oracle."""
+    if lens == "ragged32":
+        lens = synth.ragged_lens(9, 32, 1024, 40000)
+    case = synth.make_decode_case(4300 + len(lens), lens, 12, 1, extra_pages=1)
+    n = L.mla_plan_splits(len(lens), 1, 12, lens, case.block_table.shape[1], 0)
+    assert n > L.mla_auto_splits(len(lens), 1, 12, case.block_table.shape[1], 0)
+    out, lse = supported(L, impl, case.to("cuda"), n)
+    ro, rl = oracle_full(case)
+    assert_parity(out, lse, ro, rl, what=f"planned {n} partitions")
+
+
 def test_split_combine_ignores_partitions_past_each_history(L, impl):
     """The split combine counts a request's partitions past its history as empty
     whatever the scratch holds (a longest-first launch never writes them): a
