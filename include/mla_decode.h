@@ -250,8 +250,8 @@ MLA_API int32_t mla_auto_splits(int32_t B, int32_t T, int32_t H, int32_t max_pag
  * ~3/4 page each -- as the decode launches them.  Counts are tried up to 8
  * waves of full-length CTAs, and for units of up to 16 rows down to
  * partitions of 64 pages.  When host_seq_lens is NULL (or B is 0) it returns
- * mla_auto_splits(B, T, H, max_pages, sm_count).  A plan takes ~0.1-2 ms on
- * one host core, so an engine plans once per batch.
+ * mla_auto_splits(B, T, H, max_pages, sm_count).  A plan takes ~0.1-8 ms on
+ * one host core (8 ms for 4,096 requests), so an engine plans once per batch.
  *   host_seq_lens  host pointer to the B lengths the decode will read from
  *                  seq_lens (values outside [0, 64 * max_pages] are clamped).
  *   max_pages      the block table's width, as passed to the decode.
