@@ -242,12 +242,12 @@ MLA_API int32_t mla_auto_splits(int32_t B, int32_t T, int32_t H, int32_t max_pag
  * the launch on the host -- each CTA on the SM that frees first, one per SM,
  * a partition costing its pages at a fixed per-page time plus a fixed 8 pages
  * of set-up and epilogue -- and returns the count with the shortest finish
- * (ties: fewer partitions).  Units of more than 16 rows (the 32-row
- * tensor-core kernel, ceil(H * T / 32) CTAs per unit) run in launch order.
- * Units of up to 16 rows run one CTA each: in launch order while they fit the
- * SMs, and otherwise (up to 1,024 requests) longest first -- full partitions,
- * then the partial ones by length, then those past each request's history at
- * ~3/4 page each -- as the decode launches them.  Counts are tried up to 8
+ * (ties: fewer partitions).  A unit of more than 16 rows takes ceil(H * T / 32)
+ * CTAs of the 32-row tensor-core kernel, one after another; a unit of up to
+ * 16 rows one CTA.  The CTAs run in launch order while they fit the SMs, and
+ * otherwise (up to 1,024 requests) longest first -- full partitions, then the
+ * partial ones by length, then those past each request's history at ~3/4
+ * page each -- as the decode launches them.  Counts are tried up to 8
  * waves of full-length CTAs, and for units of up to 16 rows down to
  * partitions of 64 pages.  When host_seq_lens is NULL (or B is 0) it returns
  * mla_auto_splits(B, T, H, max_pages, sm_count).  A plan takes ~0.1-8 ms on

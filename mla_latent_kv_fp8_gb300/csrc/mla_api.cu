@@ -393,8 +393,9 @@ int32_t mla_auto_splits(int32_t B, int32_t T, int32_t H, int32_t max_pages, int3
 constexpr int64_t kPlanPage = 8;
 constexpr int64_t kPlanFixed = 8 * kPlanPage;
 constexpr int64_t kPlanEmpty = 6;
-// The 12-head kernel orders the units of at most this many requests longest
-// first when they outnumber the SMs (its ordering kernel's limit).
+// Both tensor-core kernels take the units of at most this many requests in
+// longest-first order when their CTAs outnumber the SMs (the ordering
+// kernel's limit).
 constexpr int32_t kLongestFirstMaxBatch = 1024;
 
 int32_t mla_plan_splits(int32_t B, int32_t T, int32_t H, const int32_t* host_seq_lens, int32_t max_pages,
@@ -461,22 +462,24 @@ int32_t mla_plan_splits(int32_t B, int32_t T, int32_t H, const int32_t* host_seq
             std::push_heap(load.begin(), load.end(), std::greater<int64_t>());
         };
         const bool longest_first =
-            narrow && cd.n > 1 && B <= kLongestFirstMaxBatch && (int64_t)B * cd.n > sm_count;
+            cd.n > 1 && B <= kLongestFirstMaxBatch && (int64_t)B * cd.n * G > sm_count;
         if (longest_first) {
             // full chunks request by request, then the partial chunks by length,
-            // then the CTAs of the partitions past each history
+            // then the CTAs of the partitions past each history; a unit's G
+            // row-CTAs start one after another
             int64_t live = 0;
             partial.clear();
             for (int32_t b = 0; b < B; ++b) {
                 const int64_t f = pages[b] / cd.chunk, r = pages[b] - f * cd.chunk;
-                for (int64_t i = 0; i < f; ++i) place(kPlanPage * cd.chunk + kPlanFixed);
+                for (int64_t i = 0; i < f * G; ++i) place(kPlanPage * cd.chunk + kPlanFixed);
                 live += f;
                 if (r > 0) partial.push_back(r);
             }
             std::sort(partial.begin(), partial.end(), std::greater<int64_t>());
-            for (int64_t r : partial) place(kPlanPage * r + kPlanFixed);
+            for (int64_t r : partial)
+                for (int64_t i = 0; i < G; ++i) place(kPlanPage * r + kPlanFixed);
             live += (int64_t)partial.size();
-            for (int64_t e = live; e < (int64_t)B * cd.n; ++e) place(kPlanEmpty);
+            for (int64_t e = live * G; e < (int64_t)B * cd.n * G; ++e) place(kPlanEmpty);
         } else {
             // launch order: partition and row-CTA fastest, then the request
             for (int32_t b = 0; b < B; ++b) {

@@ -887,7 +887,7 @@ cudaError_t encode_cache_maps(CUtensorMap* map3, CUtensorMap* map2, const uint8_
     return cudaSuccess;
 }
 
-cudaError_t launch_tc_wide(const DecodeParams& p, const CUtensorMap& map, const CUtensorMap& map_box,
+cudaError_t launch_tc_wide(const DecodeParams& p, const CUtensorMap& map, const CUtensorMap& map_box, bool lpt,
                            cudaStream_t stream);
 
 // The smallest shift S in [4, 7] with positions <= 2^(S + 6): the n positions
@@ -949,40 +949,46 @@ cudaError_t launch_tc_decode(const DecodeParams& p, cudaStream_t stream, bool* h
     // A warpgroup of the 12-head kernel accumulates every other page of a
     // partition; one of the wide kernel every page (for its rows).
     q.ref_shift = reference_shift(64ll * (HT > kNq ? p.chunk_pages : (p.chunk_pages + 1) / 2));
-    if (HT > kNq) {
-        // More than 16 rows: the wide kernel, ceil(H*T / 32) CTAs per
-        // (partition, request) with the rows shared evenly.
-        q.row_ctas = (HT + kWideRows - 1) / kWideRows;
-        q.rows_per_cta = (HT + q.row_ctas - 1) / q.row_ctas;
-        e = launch_tc_wide(q, map, map_box, stream);
-        if (e == cudaSuccess) *handled = true;
-        return e;
-    }
-    // More units than SMs (a batch of many, uneven requests): the CTAs take the
-    // units in longest-first order (schedule_units) instead of request order.
-    const long long units = (long long)p.n_splits * p.B;
-    const bool lpt = p.n_splits > 1 && p.B <= kLptMaxB && units > sms[dev];
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(p.n_splits), static_cast<unsigned>(p.B));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = sizeof(Smem) + 1024;
-    cfg.stream = stream;
     // Programmatic dependent launch: the CTAs may be scheduled while the
     // previous kernel on the stream drains; the kernel waits for it
     // (griddepcontrol.wait) before reading anything.
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (lpt) {
-        // the longest-first order, then the decode (a programmatic dependent of it)
-        cudaLaunchConfig_t ocfg = cfg;
+    // More CTAs than SMs (a batch of many, uneven requests): the CTAs take the
+    // units in longest-first order (lpt_order_kernel, launched first) instead of
+    // request order.
+    auto launch_order = [&]() {
+        cudaLaunchConfig_t ocfg = {};
         ocfg.gridDim = dim3(1);
         ocfg.blockDim = dim3(kLptThreads);
-        ocfg.dynamicSmemBytes = 0;
-        if ((e = cudaLaunchKernelEx(&ocfg, lpt_order_kernel, q)) != cudaSuccess) return e;
+        ocfg.stream = stream;
+        ocfg.attrs = attr;
+        ocfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&ocfg, lpt_order_kernel, q);
+    };
+    const long long units = (long long)p.n_splits * p.B;
+    if (HT > kNq) {
+        // More than 16 rows: the wide kernel, ceil(H*T / 32) CTAs per
+        // (partition, request) with the rows shared evenly.
+        q.row_ctas = (HT + kWideRows - 1) / kWideRows;
+        q.rows_per_cta = (HT + q.row_ctas - 1) / q.row_ctas;
+        const bool lpt = p.n_splits > 1 && p.B <= kLptMaxB && units * q.row_ctas > sms[dev];
+        if (lpt && (e = launch_order()) != cudaSuccess) return e;
+        e = launch_tc_wide(q, map, map_box, lpt, stream);
+        if (e == cudaSuccess) *handled = true;
+        return e;
     }
+    const bool lpt = p.n_splits > 1 && p.B <= kLptMaxB && units > sms[dev];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.n_splits), static_cast<unsigned>(p.B));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = sizeof(Smem) + 1024;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // the longest-first order, then the decode (a programmatic dependent of it)
+    if (lpt && (e = launch_order()) != cudaSuccess) return e;
     if (lpt)
         e = HT <= 12 ? cudaLaunchKernelEx(&cfg, tc_decode_kernel<12, true>, map, map_box, q)
                      : cudaLaunchKernelEx(&cfg, tc_decode_kernel<16, true>, map, map_box, q);

@@ -154,6 +154,7 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
 }
 
 
+template <bool kLpt>
 __global__ void __launch_bounds__(kWThreads, 1)
     tc_wide_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_box,
                    const DecodeParams p) {
@@ -166,10 +167,24 @@ __global__ void __launch_bounds__(kWThreads, 1)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     // G = p.row_ctas CTAs per (partition, request), adjacent in the grid, CTA r
     // taking rows [r * p.rows_per_cta, ...): they run at the same time, so all
-    // but the first read each page from L2.
+    // but the first read each page from L2.  In request order the grid's x is
+    // (partition, r) and y the request; with more CTAs than SMs the G CTAs of
+    // launch entry e take unit e of the longest-first order (lpt_order_kernel).
     const int G = p.row_ctas;
-    const int crank = static_cast<int>(blockIdx.x % G);
-    const int split = blockIdx.x / G, b = blockIdx.y;
+    int crank, split, b, L_known = -1;
+    if constexpr (kLpt) {
+        const long long k = (long long)blockIdx.y * gridDim.x + blockIdx.x;
+        const int2 u = p.lpt_order[k / G];
+        if (u.x < 0) return;  // past the last unit with history: nothing to do
+        crank = static_cast<int>(k % G);
+        b = u.x / p.n_splits;
+        split = u.x % p.n_splits;
+        L_known = u.y;
+    } else {
+        crank = static_cast<int>(blockIdx.x % G);
+        split = blockIdx.x / G;
+        b = blockIdx.y;
+    }
     const int r0 = p.rows_per_cta * crank;
     const int HTc = min(p.rows_per_cta, HT - r0);  // rows of this CTA (<= 32)
     volatile int* abort = &S.abort;
@@ -201,7 +216,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
             }
         }
     }
-    int L = __ldg(p.seq_lens + b);
+    int L = L_known >= 0 ? L_known : __ldg(p.seq_lens + b);
     const float kv_scale = __ldg(p.kv_scale);
     if (L < 0 || L > p.max_pages * kPage || (L > 0 && L < p.T)) {
         if (tid == 0) atomicCAS(p.err, 0, kErrSeqRange);
@@ -700,7 +715,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
 // Launch the wide kernel: p.row_ctas CTAs per (partition, request), each of at
 // most 32 rows (p.rows_per_cta); the maps are those of the 12-head kernel
 // (3-D page view and 2-D box view of the cache).
-cudaError_t launch_tc_wide(const DecodeParams& p, const CUtensorMap& map, const CUtensorMap& map_box,
+cudaError_t launch_tc_wide(const DecodeParams& p, const CUtensorMap& map, const CUtensorMap& map_box, bool lpt,
                            cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -711,7 +726,9 @@ cudaError_t launch_tc_wide(const DecodeParams& p, const CUtensorMap& map, const 
     {
         std::lock_guard<std::mutex> lk(mu);
         if (!ready[dev]) {
-            if ((e = cudaFuncSetAttribute(tc_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if ((e = cudaFuncSetAttribute(tc_wide_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)sizeof(WideSmem) + 1024)) != cudaSuccess ||
+                (e = cudaFuncSetAttribute(tc_wide_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           (int)sizeof(WideSmem) + 1024)) != cudaSuccess)
                 return e;
             ready[dev] = true;
@@ -731,7 +748,8 @@ cudaError_t launch_tc_wide(const DecodeParams& p, const CUtensorMap& map, const 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, tc_wide_kernel, map, map_box, p);
+    e = lpt ? cudaLaunchKernelEx(&cfg, tc_wide_kernel<true>, map, map_box, p)
+            : cudaLaunchKernelEx(&cfg, tc_wide_kernel<false>, map, map_box, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

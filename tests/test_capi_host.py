@@ -286,21 +286,21 @@ def test_plan_splits_for_uneven_12_head_batches(L):
 
 
 def test_plan_splits_ragged_batches(L):
-    """Short, uneven histories: the plan takes more partitions than the
-    max_pages-based count, because short requests leave SMs free.  On the
-    verify workload's 8-way DCP shards (16 requests x 48 rows, 16..195 pages)
-    it picks 7 partitions, and 16 on the whole verify workload: the fastest
-    counts of a sweep on GB300 (shards: 38.4 us at 7 against 40.6 at 6, 44.1
-    at 8 and 50.2 at the automatic 4; whole workload: 168 us at 16 against 180
-    at the automatic 14 and 212 at 18)."""
+    """Uneven histories on the 32-row kernel: the plan replays the
+    longest-first launch its CTA count triggers.  On the verify workload's 8-way
+    DCP shards (16 requests x 48 rows, 16..195 pages) and on the whole verify
+    workload it picks 8 partitions (measured on GB300: the shard rank step
+    41.5 us against 43.9 us at the 7 a request-order plan took; the whole
+    workload 160.4 us per step against 173.9 us at 16 in request order, 172.4 us
+    at 16 and 215.7 us at 8 in request order)."""
     from mla_latent_kv_fp8_gb300.dcp import shard_plan
     lens = synth.verify_lens(4)
     Lb = L
     plan = shard_plan(lens, torch.zeros((16, 2048), dtype=torch.int32), 8, 4)
     for (table, sl), (T, H) in ((plan[0], (1, 48)), (plan[-1], (4, 12))):
-        assert Lb.mla_plan_splits(16, T, H, sl.tolist(), table.shape[1], 152) == 7
+        assert Lb.mla_plan_splits(16, T, H, sl.tolist(), table.shape[1], 152) == 8
     mp = -(-max(lens) // 64)
-    assert Lb.mla_plan_splits(16, 4, 12, lens, mp, 152) == 16
+    assert Lb.mla_plan_splits(16, 4, 12, lens, mp, 152) == 8
     assert Lb.mla_auto_splits(16, 4, 12, mp, 152) == 14
 
 
@@ -323,11 +323,11 @@ def _plan_by_replay(B, T, H, lens, max_pages, sm):
     """The length-aware plan written out plainly: every candidate count (one per
     distinct chunk size, up to 8 full-length waves, and for units of at most
     16 rows partitions down to 64 pages) replayed on a min-heap of SM finish
-    times, in eighths of a page: a partition costs 8 per page plus 64, in launch
-    order; a 12-head launch of more units than SMs (at most 1,024 requests) runs
-    full chunks first, then partial chunks longest first, then the partitions
-    past each history at 6 each.  The earliest finish wins, ties to fewer
-    partitions."""
+    times, in eighths of a page: a partition costs 8 per page plus 64 on each of
+    its row-CTAs, in launch order; a launch of more CTAs than SMs (at most 1,024
+    requests) runs full chunks first, then partial chunks longest first, then
+    the partitions past each history at 6 per CTA.  The earliest finish wins,
+    ties to fewer partitions."""
     import heapq
     narrow = T * H <= 16
     G = 1 if narrow else -(-(T * H) // 32)
@@ -354,12 +354,13 @@ def _plan_by_replay(B, T, H, lens, max_pages, sm):
             finish = max(finish, t)
             heapq.heappush(heap, t)
 
-        if narrow and n > 1 and B <= 1024 and B * n > sm:
+        if n > 1 and B <= 1024 and B * n * G > sm:
             full = [chunk] * sum(p // chunk for p in pages)
             part = sorted((p % chunk for p in pages if p % chunk), reverse=True)
             for w in full + part:
-                place(8 * w + 64)
-            for _ in range(B * n - len(full) - len(part)):
+                for _ in range(G):
+                    place(8 * w + 64)
+            for _ in range((B * n - len(full) - len(part)) * G):
                 place(6)
         else:
             for p in pages:

@@ -578,10 +578,11 @@ def test_full_size_dcp_shards_and_merge(L, impl):
 
 
 # ----------------------------------------------------------------------------
-# Longest-first launches of the 12-head kernel (more units than SMs, <= 1,024
-# requests): a one-CTA kernel orders all (request, partition) units longest
-# first from the device-resident lengths and writes the empty partials; decode
-# CTA k takes entry k of that order
+# Longest-first launches (more CTAs than SMs, <= 1,024 requests): a one-CTA
+# kernel orders all (request, partition) units longest first from the
+# device-resident lengths; CTA k of the 12-head kernel takes entry k of that
+# order, and the G row-CTAs k = G e .. G e + G - 1 of the wide kernel take
+# entry e; the split combine counts the partitions past a history as empty
 # ----------------------------------------------------------------------------
 
 def _ragged(seed, B, lo, hi, zeros=0):
@@ -598,6 +599,8 @@ def _ragged(seed, B, lo, hi, zeros=0):
     (40, 4, 4, 6, 2, 2600),      # 16 rows (causal verify), 240 units
     (256, 12, 1, 2, 9, 2600),
     (1024, 12, 1, 2, 30, 500),   # the largest longest-first batch
+    (20, 12, 4, 6, 2, 2600),     # wide kernel: 48 rows (2 row-CTAs per unit), 240 CTAs
+    (12, 96, 1, 5, 1, 4000),     # wide kernel: 96 rows (3 row-CTAs per unit), 180 CTAs
     (1025, 12, 1, 2, 0, 500),    # one more request: request order
     (160, 16, 1, 1, 0, 2600),    # unsplit: one CTA per request
 ])
