@@ -55,6 +55,32 @@ def test_random_shapes_match_oracle(L, impl, seed):
     assert_parity(out, lse, ro, rl, what=f"seed {seed}: lens={lens} H={H} T={T} splits={n_splits}")
 
 
+def _draw_multiwave(seed):
+    """Batches whose launches have more CTAs than SMs: the longest-first order
+    of both kernels, at the planned, the automatic and random split counts."""
+    rng = np.random.default_rng([seed, 29])
+    T = int(rng.choice([1, 1, 2, 4]))
+    H = int(rng.choice([int(rng.integers(1, 16 // T + 1)), int(rng.integers(16 // T + 1, 128 // T + 1))]))
+    B = int(rng.integers(20, 49))
+    lens = [int(x) for x in rng.integers(T, int(rng.choice([700, 1500])), size=B)]
+    for k in range(int(rng.integers(0, 4))):
+        lens[int(rng.integers(0, B))] = 0
+    mode = seed % 3
+    return lens, H, T, mode, int(rng.integers(4, 13))
+
+
+@pytest.mark.parametrize("seed", range(18))
+def test_random_multiwave_launches_match_oracle(L, impl, seed):
+    lens, H, T, mode, explicit = _draw_multiwave(seed)
+    case = synth.make_decode_case(6000 + seed, lens, H, T, extra_pages=int(seed % 2))
+    mp = case.block_table.shape[1]
+    n_splits = (L.mla_plan_splits(len(lens), T, H, lens, mp, 0), 0, explicit)[mode]
+    out, lse = supported(L, impl, case.to("cuda"), n_splits)
+    ro, rl = oracle.decode(case.q, case.kv_cache, case.kv_scale, case.block_table, case.seq_lens,
+                           case.sm_scale)
+    assert_parity(out, lse, ro, rl, what=f"seed {seed}: B={len(lens)} H={H} T={T} splits={n_splits}")
+
+
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("seed", range(16))
 def test_random_merges_match_oracle(L, seed, dtype):
