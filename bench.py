@@ -332,11 +332,11 @@ class DecodeStep:
         self.chunk = L.mla_split_chunk_pages(mp, resolved)
         self.n_eff = -(-mp // self.chunk)
         # our kernels per step: the decode, the split combine when split, and for a
-        # 12-head tensor-core launch with more units than SMs the longest-first
-        # ordering kernel before the decode
+        # tensor-core launch with more CTAs than SMs the longest-first ordering
+        # kernel before the decode
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
-        lpt = (args.kernel != "simt" and H * T <= 16 and self.n_eff > 1
-               and B <= 1024 and B * self.n_eff > sms)
+        row_ctas = 1 if H * T <= 16 else -(-(H * T) // 32)
+        lpt = (args.kernel != "simt" and self.n_eff > 1 and B <= 1024 and B * self.n_eff * row_ctas > sms)
         self.launches_per_step = 1 + (1 if self.n_eff > 1 else 0) + (1 if lpt else 0)
         self.graph = None
         self.gsteps = self.n_copies * max(1, -(-16 // self.n_copies))
@@ -510,6 +510,29 @@ def run_ours(args):
         rows_ctas = 1 if H * T <= 16 else -(-(H * T) // 32)  # CTAs per (request, partition)
         ceiling = stream_ceiling(L, base, w.caches, w.n_copies, B * w.n_eff * rows_ctas, stream)
 
+    # ---- the count a caller without host lengths gets (mla_auto_splits), for comparison ----
+    split_plan = None
+    auto_n = L.mla_auto_splits(B, T, H, base.block_table.shape[1], 0)
+    if w.planner.startswith("mla_plan_splits") and auto_n != w.n_eff:
+        keep = (w.n_splits, w.graph)
+        w.n_splits = auto_n
+        for i in range(3):  # grows the stream's scratch outside any capture
+            w.step(i)
+        barrier()
+        w.capture()
+        barrier()
+        k_auto = max(200, w.gsteps)
+        ms_a, _, _ = w.timed(k_auto, barrier)
+        ms_a = max_over_ranks(ms_a, world, dev) / k_auto
+        assert L.mla_device_error() == 0
+        w.n_splits, w.graph = keep
+        split_plan = {
+            "planned": {"n_splits": w.n_eff, "us_per_step": round(ms_step * 1e3, 2)},
+            "automatic": {"n_splits": auto_n, "us_per_step": round(ms_a * 1e3, 2),
+                          "value": round(job_gbps(kv_bytes, world, ms_a), 1), "unit": "GB/s", "steps": k_auto},
+            "note": "the same step at mla_auto_splits' count (from max_pages alone: what a caller without "
+                    "host lengths gets), graph-replayed after the timed region"}
+
     # ---- the other part of the serving mix, measured the same way ----
     side = {}
     for name in others:
@@ -608,6 +631,7 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "e2e": e2e,
             "stream_ceiling": ceiling,
+            "split_plan": split_plan,
             "append": append,
             "dcp_merge": dcp_merge,
             "dcp_verify": dcp_verify,
