@@ -225,15 +225,14 @@ MLA_API mla_status_t mla_append_latent(const mla_tensor_t *latent, const float *
                                const mla_tensor_t *block_table, const mla_tensor_t *start_pos,
                                const mla_tensor_t *kv_cache, void *stream);
 
-/* The automatic split count used when n_splits == 0: enough history
- * partitions per request that B * splits fills every SM of the device
- * (at least one full wave), with at least 2 pages (128 positions) each.
- * Units of more than 16 rows run on the wide tensor-core kernel, 32 rows per
- * CTA: a (request, partition) unit then takes ceil(H * T / 32) CTAs, and when
- * that is more than one the count minimises the number of waves of CTAs
- * times the partition length.  Partitions never exceed 160 pages
- * (10,240 positions), so that in a batch of mixed lengths the longest request
- * does not bound the call.
+/* The automatic split count used when n_splits == 0, from max_pages alone
+ * (every request taken as max_pages long): the count that minimises the number
+ * of waves of CTAs times (the partition length + a fixed 8 pages per CTA),
+ * with at least 2 pages (128 positions) per partition.  A (request,
+ * partition) unit takes one CTA of the 12-head tensor-core kernel for up to 16
+ * rows, and ceil(H * T / 32) CTAs of the 32-row kernel beyond.  Partitions
+ * never exceed 160 pages (10,240 positions), so that in a batch of mixed
+ * lengths the longest request does not bound the call.
  * Pure host function; sm_count <= 0 means "query the current device". */
 MLA_API int32_t mla_auto_splits(int32_t B, int32_t T, int32_t H, int32_t max_pages, int32_t sm_count);
 

@@ -53,7 +53,10 @@ def test_status_strings(L):
     (1, 6144, 152, 150),    # one request x 393K: >= SM count partitions
     (1, 16, 152, 8),        # short history: partitions of >= 2 pages
     (1, 2, 152, 1),
-    (200, 100, 152, 1),     # more requests than SMs: no split
+    (200, 100, 152, 3),     # more requests than SMs: 4 waves of 34-page partitions beat 2 unsplit
+    (16, 512, 152, 9),      # 144 units in one wave (ceil(152 / 16) = 10 would spill 8 into a second)
+    (32, 512, 152, 9),      # 288 units: two nearly full waves of 57 pages
+    (128, 2219, 152, 14),   # the ragged mix's table: 160-page partitions
 ])
 def test_auto_splits(L, B, max_pages, sm, expect):
     s = L.mla_auto_splits(B, 1, 12, max_pages, sm)
