@@ -1,5 +1,5 @@
 """The cross-GPU DCP exchange (mla_latent_kv_fp8_gb300.dcp) on CPU ranks (gloo,
-world size 2): section 1 "Cache", DCP paragraph of the post -- every rank holds
+world sizes 2 and 3): section 1 "Cache", DCP paragraph of the post -- every rank holds
 one contiguous shard of every history; the queries are all-gathered so every
 rank attends with all heads to its shard; the partial answers (out, lse) are
 all-gathered and merged by their normalisers.
@@ -73,9 +73,10 @@ def _rank_main(rank, world, port, q_full, partials, dtype, result):
         dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("T,dtype", [(1, torch.float64), (4, torch.float64), (4, torch.bfloat16)])
-def test_dcp_exchange_matches_unsharded_oracle(T, dtype):
-    world, H = 2, 12
+@pytest.mark.parametrize("world,T,dtype", [(2, 1, torch.float64), (2, 4, torch.float64), (2, 4, torch.bfloat16),
+                                           (3, 4, torch.float64)])
+def test_dcp_exchange_matches_unsharded_oracle(world, T, dtype):
+    H = 12
     lens = [1500, 700, 900]
     case = synth.make_decode_case(41 + T, lens, H, T, extra_pages=3)
     plan = dcp.shard_plan(lens, case.block_table, world, T)
