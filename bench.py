@@ -526,6 +526,9 @@ def run_ours(args):
         ms_a = max_over_ranks(ms_a, world, dev) / k_auto
         assert L.mla_device_error() == 0
         w.n_splits, w.graph = keep
+        with torch.cuda.stream(stream):  # w.out holds the planned count's answer again
+            w.graph.replay()
+        barrier()
         split_plan = {
             "planned": {"n_splits": w.n_eff, "us_per_step": round(ms_step * 1e3, 2)},
             "automatic": {"n_splits": auto_n, "us_per_step": round(ms_a * 1e3, 2),
