@@ -363,7 +363,7 @@ int32_t mla_auto_splits(int32_t B, int32_t T, int32_t H, int32_t max_pages, int3
     // G CTAs per unit (1 for the 12-head kernel): the count that minimises waves
     // of CTAs x (pages per partition + a fixed cost of ~8 pages per CTA),
     // assuming every request is max_pages long.  A count that overshoots a wave
-    // by a few units (e.g. ceil(SMs / B) units per request) pays a second wave.
+    // by a few units (e.g. ceil(SMs / B) partitions per request) pays a second wave.
     int64_t best = -1, s = 1;
     for (int64_t c = 1; c <= most && c <= 1024; ++c) {
         const int64_t cost = ceil_div(B * c * G, sm_count) * (ceil_div(max_pages, c) + 8);
